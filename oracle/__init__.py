@@ -1,0 +1,161 @@
+"""CPU oracle for the left-balanced k-d tree build (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  The CUDA library never imports it and
+shares no code with it.  Every function here is a thin ctypes wrapper around
+``kdt_oracle.c``; see that file's header for the passages each routine follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kdt_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+
+OK = 0
+EINVAL = -1
+ENOMEM = -2
+ENONFINITE = -4
+EINTERNAL = -6
+
+
+def library_path(mutant: int = 0) -> str:
+    name = "libkdt_oracle.so" if mutant == 0 else f"libkdt_oracle_m{mutant}.so"
+    return os.path.join(_BUILD_DIR, name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FP contraction).
+
+    ``mutant`` > 0 plants one deliberate mistake (used only by the tests that
+    show the pins catch it)."""
+    out = library_path(mutant)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD_DIR)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", f"-DKDO_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """Typed handle on one compiled oracle (the real one, or a mutant)."""
+
+    def __init__(self, mutant: int = 0):
+        self.mutant = mutant
+        self.lib = ctypes.CDLL(build(mutant))
+        L = self.lib
+        i64, i32, f32p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.kdo_level.argtypes = [i64]
+        L.kdo_level.restype = i32
+        L.kdo_num_levels.argtypes = [i64]
+        L.kdo_num_levels.restype = i32
+        L.kdo_subtree_count.argtypes = [i64, i64]
+        L.kdo_subtree_count.restype = i64
+        L.kdo_less.argtypes = [f32p, i32, i32, i64, i64]
+        L.kdo_less.restype = i32
+        L.kdo_widest_dim.argtypes = [f32p, f32p, i32]
+        L.kdo_widest_dim.restype = i32
+        L.kdo_build.argtypes = [f32p, i64, i32, i32, f32p]
+        L.kdo_build.restype = i32
+        L.kdo_verify.argtypes = [f32p, i64, i32, i32, f32p, f32p, i64, i32,
+                                 ctypes.POINTER(ctypes.c_int64)]
+        L.kdo_verify.restype = i32
+        L.kdo_brute_force.argtypes = [f32p, i32, i32, i32, f32p]
+        L.kdo_brute_force.restype = i64
+
+    # -- notation ---------------------------------------------------------
+    def level(self, i: int) -> int:
+        return self.lib.kdo_level(i)
+
+    def num_levels(self, n: int) -> int:
+        return self.lib.kdo_num_levels(n)
+
+    def subtree_count(self, n: int, t: int) -> int:
+        return self.lib.kdo_subtree_count(n, t)
+
+    # -- order / split rule -----------------------------------------------
+    def less(self, pts: np.ndarray, p: int, a: int, b: int) -> bool:
+        pts = _points(pts)
+        return bool(self.lib.kdo_less(pts.ctypes.data, pts.shape[1], p, a, b))
+
+    def widest_dim(self, lo: np.ndarray, hi: np.ndarray) -> int:
+        lo = np.ascontiguousarray(lo, dtype=np.float32)
+        hi = np.ascontiguousarray(hi, dtype=np.float32)
+        return self.lib.kdo_widest_dim(lo.ctypes.data, hi.ctypes.data, lo.size)
+
+    # -- build / verify -----------------------------------------------------
+    def build_tree(self, pts: np.ndarray, mode: int = 0) -> np.ndarray:
+        pts = _points(pts)
+        n, k = pts.shape
+        perm = np.empty(n, dtype=np.int32)
+        rc = self.lib.kdo_build(pts.ctypes.data, n, k, mode, perm.ctypes.data)
+        if rc != OK:
+            raise OracleError(rc)
+        return perm
+
+    def verify(self, pts: np.ndarray, perm: np.ndarray, mode: int = 0,
+               nodes: np.ndarray | None = None, check_perm: bool = True):
+        """Returns (ok, bad_node).  bad_node == -1 flags a non-permutation."""
+        pts = _points(pts)
+        n, k = pts.shape
+        perm = np.ascontiguousarray(perm, dtype=np.int32)
+        if perm.shape != (n,):
+            raise ValueError("perm must have shape (N,)")
+        bad = ctypes.c_int64(-2)
+        if nodes is None:
+            rc = self.lib.kdo_verify(pts.ctypes.data, n, k, mode, perm.ctypes.data,
+                                     None, 0, int(check_perm), ctypes.byref(bad))
+        else:
+            nodes = np.ascontiguousarray(nodes, dtype=np.int64)
+            rc = self.lib.kdo_verify(pts.ctypes.data, n, k, mode, perm.ctypes.data,
+                                     nodes.ctypes.data, nodes.size, int(check_perm),
+                                     ctypes.byref(bad))
+        if rc < 0:
+            raise OracleError(rc)
+        return rc == 0, int(bad.value)
+
+    def brute_force(self, pts: np.ndarray, mode: int = 0):
+        """Returns (number of valid orderings, first valid ordering)."""
+        pts = _points(pts)
+        n, k = pts.shape
+        first = np.full(n, -1, dtype=np.int32)
+        cnt = self.lib.kdo_brute_force(pts.ctypes.data, n, k, mode, first.ctypes.data)
+        if cnt < 0:
+            raise OracleError(int(cnt))
+        return int(cnt), first
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"oracle returned error code {code}")
+        self.code = code
+
+
+def _points(pts: np.ndarray) -> np.ndarray:
+    pts = np.ascontiguousarray(pts, dtype=np.float32)
+    if pts.ndim != 2:
+        raise ValueError("points must be an (N, k) array")
+    return pts
+
+
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The (unmutated) oracle, compiled on first use."""
+    global _default
+    if _default is None:
+        _default = Oracle(0)
+    return _default

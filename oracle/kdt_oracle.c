@@ -1,0 +1,413 @@
+/*
+ * kdt_oracle.c -- CPU oracle for the left-balanced, complete, level-order k-d tree.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously-correct
+ * reference that the CUDA build is checked against.  Only the test suite, the
+ * package's smoke() check and bench.py's CPU-baseline / reference leg may load
+ * it.  It shares no code, header, table or helper with the CUDA library, and
+ * the CUDA library never calls it.
+ *
+ * Sources (cited by page title and passage):
+ *   [W]  "GPU-friendly, Parallel, and (Almost-)In-Place Construction of
+ *        Left-Balanced k-d Trees" (Wald, arXiv 2211.00120):
+ *          - problem paragraph: k-d condition (left subtree <=, right >= in the
+ *            node's split dimension) plus the left-balanced shape;
+ *          - notation paragraph: level-order ids, parent/lChild/rChild,
+ *            level(i), numLevels(N);
+ *          - round-robin paragraph: split dimension l mod k for level l;
+ *          - split-widest-dimension paragraphs: domain = bounding box of the
+ *            whole data set clipped by the ancestors' split planes, split
+ *            dimension = widest extent of that domain.
+ *   [R]  "An Implementation of a Balanced Kd Tree Builder Using GPUs"
+ *        (Robinson, KdTreeGPU wiki), sort paragraph: on equal primary
+ *        coordinates compare the next coordinate, then the next, ... (the
+ *        "super key").
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - the super key is cyclic from the split dimension p: (x[p], x[p+1 mod k],
+ *     ..., x[p-1 mod k]) and, when all coordinates are equal, the original
+ *     input index breaks the tie; this makes the order strict and total, so
+ *     the tree is unique;
+ *   - float comparison uses IEEE '<' (so -0 == +0);
+ *   - the split point of subtree s is the element of 0-based rank
+ *     |S(lChild(s))| of s's point set under that order;
+ *   - widest mode: extent = hi - lo in float32 round-to-nearest; the lowest
+ *     dimension wins ties (strict '>' to replace); the domain of a child is the
+ *     parent's domain with hi[d] (left) or lo[d] (right) set to the split
+ *     point's coordinate;
+ *   - non-finite coordinates are rejected.
+ *
+ * Not reentrant: the qsort comparator reads a file-scope context.  The oracle
+ * is single-threaded by design.
+ *
+ * Mutants: compiling with -DKDO_MUTANT=<n> plants one deliberate mistake (see
+ * the KDO_MUTANT blocks).  The test suite builds each mutant and checks that
+ * at least one pin fails; the product build never defines it.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#ifndef KDO_MUTANT
+#define KDO_MUTANT 0
+#endif
+
+#define KDO_OK 0
+#define KDO_EINVAL (-1)
+#define KDO_ENOMEM (-2)
+#define KDO_ENONFINITE (-4)
+#define KDO_EINTERNAL (-6)
+#define KDO_MAXK 32
+
+/* ---- tree notation ([W] notation paragraph) ------------------------------ */
+
+/* level(i) = floor(log2(i+1)), written as a loop. */
+int kdo_level(int64_t i)
+{
+    int l = 0;
+    uint64_t v = (uint64_t)i + 1u;
+    while (v > 1u) {
+        v >>= 1;
+        l++;
+    }
+    return l;
+}
+
+/* numLevels(N) = level(N-1) + 1. */
+int kdo_num_levels(int64_t N)
+{
+    return kdo_level(N - 1) + 1;
+}
+
+/* |S(t)|: number of nodes of the subtree rooted at t in the level-order tree
+ * of N nodes.  Counted level by level: the depth-j descendants of t are the
+ * 2^j consecutive ids starting at 2^j (t+1) - 1; count the ones below N.
+ * (Deliberately not the closed form that the CUDA library uses.) */
+int64_t kdo_subtree_count(int64_t N, int64_t t)
+{
+    int64_t total = 0;
+    if (t < 0 || t >= N)
+        return 0;
+    for (int j = 0; j < 63; j++) {
+        int64_t first = ((t + 1) << j) - 1;
+        int64_t width = (int64_t)1 << j;
+        if (first >= N)
+            break;
+        int64_t have = N - first;
+        total += have < width ? have : width;
+        if ((t + 1) > (INT64_MAX >> (j + 1)))
+            break;
+    }
+    return total;
+}
+
+/* ---- the strict total order <_p ([R] super key + index reading) ---------- */
+
+/* Returns 1 if point a precedes point b under <_p, else 0. */
+int kdo_less(const float *pts, int k, int p, int64_t a, int64_t b)
+{
+    for (int j = 0; j < k; j++) {
+#if KDO_MUTANT == 2
+        int c = j; /* mutant: non-cyclic super key */
+#else
+        int c = (p + j) % k;
+#endif
+        float xa = pts[a * k + c];
+        float xb = pts[b * k + c];
+        if (xa < xb)
+            return 1;
+        if (xb < xa)
+            return 0;
+    }
+#if KDO_MUTANT == 3
+    return a > b; /* mutant: index tiebreak reversed */
+#else
+    return a < b;
+#endif
+}
+
+/* Widest extent of a domain ([W] split-widest-dimension paragraphs): argmax of
+ * hi[d] - lo[d] in float32, lowest d on ties. */
+int kdo_widest_dim(const float *lo, const float *hi, int k)
+{
+    int best = 0;
+    float ext = hi[0] - lo[0];
+    for (int d = 1; d < k; d++) {
+        float e = hi[d] - lo[d];
+#if KDO_MUTANT == 4
+        if (e >= ext) { /* mutant: highest dimension wins ties */
+#else
+        if (e > ext) {
+#endif
+            ext = e;
+            best = d;
+        }
+    }
+    return best;
+}
+
+/* ---- recursive median-split builder --------------------------------------- */
+
+static const float *g_pts;
+static int g_k;
+static int g_p;
+
+static int cmp_idx(const void *va, const void *vb)
+{
+    int32_t a = *(const int32_t *)va;
+    int32_t b = *(const int32_t *)vb;
+    if (kdo_less(g_pts, g_k, g_p, a, b))
+        return -1;
+    if (kdo_less(g_pts, g_k, g_p, b, a))
+        return 1;
+    return 0;
+}
+
+typedef struct {
+    const float *pts;
+    int64_t N;
+    int k;
+    int mode;
+    int32_t *perm;
+    int bad; /* set if a subtree received the wrong number of points */
+} build_ctx;
+
+/* rec(s, P, dom): P holds exactly the points of subtree s.  Sort P under the
+ * split order of s, place the element of rank |S(lChild(s))| at node s, and
+ * recurse on the two sides with the clipped domains. */
+static void rec(build_ctx *c, int64_t s, int32_t *P, int64_t n,
+                const float *lo, const float *hi)
+{
+    if (n == 0)
+        return;
+    if (s >= c->N || n != kdo_subtree_count(c->N, s)) {
+        c->bad = 1; /* cannot happen for the real oracle; keeps mutants in bounds */
+        return;
+    }
+    int d;
+    if (c->mode == 0) {
+#if KDO_MUTANT == 7
+        d = (kdo_level(s) + 1) % c->k; /* mutant: wrong round-robin phase */
+#else
+        d = kdo_level(s) % c->k;
+#endif
+    } else {
+        d = kdo_widest_dim(lo, hi, c->k);
+    }
+#if KDO_MUTANT == 1
+    int64_t m = kdo_subtree_count(c->N, 2 * s + 1);
+    if (m + 1 < n)
+        m += 1; /* mutant: split rank off by one */
+#else
+    int64_t m = kdo_subtree_count(c->N, 2 * s + 1);
+#endif
+    g_pts = c->pts;
+    g_k = c->k;
+    g_p = d;
+    qsort(P, (size_t)n, sizeof(int32_t), cmp_idx);
+    c->perm[s] = P[m];
+    float split = c->pts[(int64_t)P[m] * c->k + d];
+
+    float clo[KDO_MAXK], chi[KDO_MAXK];
+    memcpy(clo, lo, sizeof(float) * c->k);
+    memcpy(chi, hi, sizeof(float) * c->k);
+#if KDO_MUTANT == 6
+    clo[d] = split; /* mutant: left child clipped on the wrong side */
+#else
+    chi[d] = split;
+#endif
+#if KDO_MUTANT == 5
+    rec(c, 2 * s + 1, P + m + 1, n - m - 1, clo, chi); /* mutant: sides swapped */
+#else
+    rec(c, 2 * s + 1, P, m, clo, chi);
+#endif
+
+    memcpy(clo, lo, sizeof(float) * c->k);
+    memcpy(chi, hi, sizeof(float) * c->k);
+    clo[d] = split;
+#if KDO_MUTANT == 5
+    rec(c, 2 * s + 2, P, m, clo, chi);
+#else
+    rec(c, 2 * s + 2, P + m + 1, n - m - 1, clo, chi);
+#endif
+}
+
+static int check_args(const float *pts, int64_t N, int k, int mode)
+{
+    if (!pts || N < 1 || N > INT32_MAX || k < 1 || k > KDO_MAXK ||
+        (mode != 0 && mode != 1))
+        return KDO_EINVAL;
+    for (int64_t i = 0; i < N * (int64_t)k; i++)
+        if (!isfinite(pts[i]))
+            return KDO_ENONFINITE;
+    return KDO_OK;
+}
+
+/* Bounding box of all points: the root domain ([W] widest-dimension init). */
+static void bbox(const float *pts, int64_t N, int k, float *lo, float *hi)
+{
+    for (int d = 0; d < k; d++) {
+        lo[d] = pts[d];
+        hi[d] = pts[d];
+    }
+    for (int64_t i = 1; i < N; i++)
+        for (int d = 0; d < k; d++) {
+            float x = pts[i * k + d];
+            if (x < lo[d])
+                lo[d] = x;
+            if (hi[d] < x)
+                hi[d] = x;
+        }
+}
+
+/* perm[node] = input index of the point stored at level-order node `node`. */
+int kdo_build(const float *pts, int64_t N, int k, int mode, int32_t *perm)
+{
+    int rc = check_args(pts, N, k, mode);
+    if (rc != KDO_OK)
+        return rc;
+    if (!perm)
+        return KDO_EINVAL;
+    int32_t *P = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+    if (!P)
+        return KDO_ENOMEM;
+    for (int64_t i = 0; i < N; i++)
+        P[i] = (int32_t)i;
+    float lo[KDO_MAXK], hi[KDO_MAXK];
+    bbox(pts, N, k, lo, hi);
+    build_ctx c = {pts, N, k, mode, perm, 0};
+    for (int64_t i = 0; i < N; i++)
+        perm[i] = -1;
+    rec(&c, 0, P, N, lo, hi);
+    free(P);
+    return c.bad ? KDO_EINTERNAL : KDO_OK;
+}
+
+/* ---- verifier: the definition checked node against every ancestor -------- */
+
+/* Checks node i against each of its ancestors a: if i lies in the left
+ * subtree of a then perm[i] <_{d(a)} perm[a], else perm[a] <_{d(a)} perm[i].
+ * d(a) is recomputed while walking down from the root (round-robin: level mod
+ * k; widest: the domain is clipped by each visited ancestor's split point).
+ * Returns 1 if the node satisfies all its conditions. */
+static int node_ok(const float *pts, int64_t N, int k, int mode,
+                   const int32_t *perm, int64_t i, const float *rlo,
+                   const float *rhi)
+{
+    float lo[KDO_MAXK], hi[KDO_MAXK];
+    memcpy(lo, rlo, sizeof(float) * k);
+    memcpy(hi, rhi, sizeof(float) * k);
+    int depth = kdo_level(i);
+    int64_t a = 0;
+    for (int j = 0; j < depth; j++) {
+        int right = (int)(((uint64_t)(i + 1) >> (depth - 1 - j)) & 1u);
+        int d = mode == 0 ? kdo_level(a) % k : kdo_widest_dim(lo, hi, k);
+        int64_t pa = perm[a], pi = perm[i];
+        if (pa < 0 || pa >= N || pi < 0 || pi >= N)
+            return 0;
+        if (right) {
+            if (!kdo_less(pts, k, d, pa, pi))
+                return 0;
+            lo[d] = pts[pa * k + d];
+        } else {
+            if (!kdo_less(pts, k, d, pi, pa))
+                return 0;
+            hi[d] = pts[pa * k + d];
+        }
+        a = 2 * a + 1 + right;
+    }
+    return 1;
+}
+
+/* Verifies the given nodes (all nodes if nodes == NULL) and, when check_perm is
+ * set, that perm is a permutation of 0..N-1.  Returns 0 if valid, 1 if not
+ * (first failing node in *bad_node, or -1 for a permutation failure), <0 on
+ * error. */
+int kdo_verify(const float *pts, int64_t N, int k, int mode,
+               const int32_t *perm, const int64_t *nodes, int64_t count,
+               int check_perm, int64_t *bad_node)
+{
+    int rc = check_args(pts, N, k, mode);
+    if (rc != KDO_OK)
+        return rc;
+    if (!perm)
+        return KDO_EINVAL;
+    if (bad_node)
+        *bad_node = -2;
+    if (check_perm) {
+        unsigned char *seen = (unsigned char *)calloc((size_t)N, 1);
+        if (!seen)
+            return KDO_ENOMEM;
+        for (int64_t i = 0; i < N; i++) {
+            int64_t p = perm[i];
+            if (p < 0 || p >= N || seen[p]) {
+                free(seen);
+                if (bad_node)
+                    *bad_node = -1;
+                return 1;
+            }
+            seen[p] = 1;
+        }
+        free(seen);
+    }
+    float lo[KDO_MAXK], hi[KDO_MAXK];
+    bbox(pts, N, k, lo, hi);
+    int64_t n = nodes ? count : N;
+    for (int64_t t = 0; t < n; t++) {
+        int64_t i = nodes ? nodes[t] : t;
+        if (i < 0 || i >= N)
+            return KDO_EINVAL;
+        if (!node_ok(pts, N, k, mode, perm, i, lo, hi)) {
+            if (bad_node)
+                *bad_node = i;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+/* ---- exhaustive search over all orderings (tiny N) ------------------------ */
+
+/* Counts the orderings of 0..N-1 that satisfy the tree conditions (every node
+ * against every ancestor); copies the first valid one to first_valid.
+ * Heap's algorithm enumerates all N! orderings.  N <= 11. */
+int64_t kdo_brute_force(const float *pts, int N, int k, int mode,
+                        int32_t *first_valid)
+{
+    if (check_args(pts, N, k, mode) != KDO_OK || N > 11)
+        return -1;
+    int32_t a[11];
+    int c[11];
+    for (int i = 0; i < N; i++) {
+        a[i] = i;
+        c[i] = 0;
+    }
+    float lo[KDO_MAXK], hi[KDO_MAXK];
+    bbox(pts, N, k, lo, hi);
+    int64_t valid = 0;
+    for (;;) {
+        int ok = 1;
+        for (int64_t i = 0; i < N && ok; i++)
+            ok = node_ok(pts, N, k, mode, a, i, lo, hi);
+        if (ok) {
+            if (valid == 0 && first_valid)
+                memcpy(first_valid, a, sizeof(int32_t) * N);
+            valid++;
+        }
+        /* next permutation (Heap's algorithm, iterative form) */
+        int i = 1;
+        while (i < N && c[i] >= i) {
+            c[i] = 0;
+            i++;
+        }
+        if (i >= N)
+            break;
+        int j = (i % 2 == 0) ? 0 : c[i];
+        int32_t tmp = a[j];
+        a[j] = a[i];
+        a[i] = tmp;
+        c[i]++;
+    }
+    return valid;
+}
