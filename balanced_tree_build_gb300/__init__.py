@@ -1,1 +1,232 @@
-"""GB300-native builder for left-balanced, complete, level-order k-d trees."""
+"""GB300-native builder for left-balanced, complete, level-order k-d trees.
+
+Thin Python binding over the C ABI in ``include/kdtree_build.h``: the
+functions here only check and marshal arguments (torch tensors give device
+memory and the current CUDA stream); every step of the build runs in the
+library's CUDA kernels.  There is no CPU fallback: if the compiled library is
+missing, the calls raise.
+
+    import torch, balanced_tree_build_gb300 as kdt
+    pts = torch.rand(1_000_000, 3, device="cuda")
+    perm = kdt.build_tree(pts)          # int32 [N]: perm[node] = input index
+    assert kdt.verify_tree(pts, perm)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+SPLIT_ROUND_ROBIN = 0
+SPLIT_WIDEST = 1
+
+OK = 0
+EINVAL = -1
+ENOMEM = -2
+ECUDA = -3
+ENONFINITE = -4
+ETIMEOUT = -5
+EINTERNAL = -6
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkdtree_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kdtree_build.h")
+
+_lib = None
+
+
+class KdtError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = _error_string(code)
+        super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
+
+
+class _KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double), ("bytes_alg", ctypes.c_double)]
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"CUDA library not built ({LIB_PATH} missing); run "
+            "`python -m balanced_tree_build_gb300._build` first")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.kdt_workspace_size.argtypes = [i64, i32, i32, ctypes.POINTER(sz)]
+    L.kdt_host_workspace_size.argtypes = [i64, i32, i32, ctypes.POINTER(sz)]
+    L.kdt_build.argtypes = [vp, i64, i32, i32, vp, vp]
+    L.kdt_build_ws.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
+    L.kdt_build_host.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
+    L.kdt_verify.argtypes = [vp, i64, i32, i32, vp, vp]
+    L.kdt_status.argtypes = [vp]
+    L.kdt_error_string.argtypes = [i32]
+    L.kdt_error_string.restype = ctypes.c_char_p
+    L.kdt_profile_enable.argtypes = [i32]
+    L.kdt_profile_read.argtypes = [ctypes.POINTER(_KernelStat), i32]
+    for name in ("kdt_workspace_size", "kdt_host_workspace_size", "kdt_build", "kdt_build_ws",
+                 "kdt_build_host", "kdt_verify", "kdt_status", "kdt_profile_enable",
+                 "kdt_profile_reset", "kdt_profile_read"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def lib():
+    """The loaded ctypes library (raises if it was not built)."""
+    return _load()
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions declared in include/kdtree_build.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kdt_\w+)\s*\(", text, re.M)))
+
+
+def _error_string(code: int) -> str:
+    try:
+        return _load().kdt_error_string(code).decode()
+    except Exception:  # library missing: still produce a message
+        return {0: "ok", -1: "invalid argument", -2: "out of memory", -3: "CUDA error",
+                -4: "non-finite coordinate", -5: "timeout", -6: "internal error"}.get(code, "error")
+
+
+def _check(rc: int, what: str) -> int:
+    if rc < 0:
+        raise KdtError(rc, what)
+    return rc
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_points(points):
+    import torch
+    if not isinstance(points, torch.Tensor):
+        raise TypeError("points must be a torch.Tensor")
+    if not points.is_cuda:
+        raise ValueError("points must be a CUDA tensor (use build_tree_host for host data)")
+    if points.dtype != torch.float32 or points.dim() != 2 or not points.is_contiguous():
+        raise ValueError("points must be a contiguous float32 tensor of shape (N, k)")
+    return points.shape[0], points.shape[1]
+
+
+def workspace_bytes(n: int, k: int, mode: int = SPLIT_ROUND_ROBIN) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_load().kdt_workspace_size(n, k, mode, ctypes.byref(out)), "kdt_workspace_size")
+    return int(out.value)
+
+
+def host_workspace_bytes(n: int, k: int, mode: int = SPLIT_ROUND_ROBIN) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_load().kdt_host_workspace_size(n, k, mode, ctypes.byref(out)), "kdt_host_workspace_size")
+    return int(out.value)
+
+
+def alloc_workspace(n: int, k: int, mode: int = SPLIT_ROUND_ROBIN, device=None, host: bool = False):
+    """A device byte tensor big enough for kdt_build_ws (or kdt_build_host)."""
+    import torch
+    nbytes = host_workspace_bytes(n, k, mode) if host else workspace_bytes(n, k, mode)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def build_tree(points, mode: int = SPLIT_ROUND_ROBIN, out=None, workspace=None, stream=None):
+    """Builds the tree of ``points`` (CUDA float32 [N, k]) and returns int32
+    [N] with perm[node] = input index.  Stream-ordered on ``stream`` (default:
+    torch's current stream).  With ``workspace`` (from alloc_workspace) the
+    call allocates nothing; otherwise the library allocates stream-ordered."""
+    import torch
+    n, k = _check_points(points)
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=points.device)
+    elif out.dtype != torch.int32 or out.shape != (n,) or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA int32 tensor of shape (N,)")
+    L = _load()
+    s = _stream_ptr(stream)
+    if workspace is None:
+        rc = L.kdt_build(ctypes.c_void_p(points.data_ptr()), n, k, mode,
+                         ctypes.c_void_p(out.data_ptr()), s)
+    else:
+        rc = L.kdt_build_ws(ctypes.c_void_p(points.data_ptr()), n, k, mode,
+                            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                            workspace.numel() * workspace.element_size(), s)
+    _check(rc, "kdt_build")
+    return out
+
+
+def build_tree_host(points, mode: int = SPLIT_ROUND_ROBIN, out=None, workspace=None, stream=None):
+    """Host-buffer build: ``points`` is a host float32 [N, k] array (numpy or
+    CPU tensor; pinned memory copies asynchronously), the result a host int32
+    array.  Synchronous."""
+    import numpy as np
+    import torch
+    if isinstance(points, np.ndarray):
+        pts = np.ascontiguousarray(points, dtype=np.float32)
+        ptr, n, k = pts.ctypes.data, pts.shape[0], pts.shape[1]
+        keep = pts
+    else:
+        if points.is_cuda or points.dtype != torch.float32 or points.dim() != 2 or not points.is_contiguous():
+            raise ValueError("points must be a contiguous host float32 (N, k) array")
+        ptr, n, k = points.data_ptr(), points.shape[0], points.shape[1]
+        keep = points
+    if out is None:
+        out = np.empty(n, dtype=np.int32)
+    optr = out.ctypes.data if isinstance(out, np.ndarray) else out.data_ptr()
+    if workspace is None:
+        workspace = alloc_workspace(n, k, mode, host=True)
+    rc = _load().kdt_build_host(ctypes.c_void_p(ptr), n, k, mode, ctypes.c_void_p(optr),
+                                ctypes.c_void_p(workspace.data_ptr()),
+                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    del keep
+    _check(rc, "kdt_build_host")
+    return out
+
+
+def verify_tree(points, perm, mode: int = SPLIT_ROUND_ROBIN, stream=None) -> bool:
+    """True iff ``perm`` is the tree of ``points`` (every node against every
+    ancestor, plus the permutation check).  Synchronous."""
+    import torch
+    n, k = _check_points(points)
+    if perm.dtype != torch.int32 or perm.shape != (n,) or not perm.is_cuda or not perm.is_contiguous():
+        raise ValueError("perm must be a contiguous CUDA int32 tensor of shape (N,)")
+    rc = _load().kdt_verify(ctypes.c_void_p(points.data_ptr()), n, k, mode,
+                            ctypes.c_void_p(perm.data_ptr()), _stream_ptr(stream))
+    _check(rc, "kdt_verify")
+    return rc == 0
+
+
+def status(stream=None) -> int:
+    """Synchronises, then returns and clears the device status word."""
+    return int(_load().kdt_status(_stream_ptr(stream)))
+
+
+def check_status(stream=None) -> None:
+    rc = status(stream)
+    if rc != OK:
+        raise KdtError(rc, "device status")
+
+
+def profile_enable(on: bool = True) -> None:
+    _load().kdt_profile_enable(1 if on else 0)
+
+
+def profile_reset() -> None:
+    _load().kdt_profile_reset()
+
+
+def profile_read() -> list[dict]:
+    L = _load()
+    buf = (_KernelStat * 64)()
+    n = L.kdt_profile_read(buf, 64)
+    return [{"name": buf[i].name.decode(), "launches": int(buf[i].launches),
+             "total_ms": float(buf[i].total_ms), "bytes_alg": float(buf[i].bytes_alg)}
+            for i in range(min(n, 64))]

@@ -1,0 +1,236 @@
+// kdt_api.cu -- the C ABI (include/kdtree_build.h): argument checks,
+// workspace handling, the per-device status word and per-kernel timing.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kdt_internal.cuh"
+
+namespace kdt {
+
+// Sticky per-device status word (each device that loads the module has its own).
+__device__ int g_device_status;
+
+__global__ void status_fold_kernel(const int *s) {
+    const int v = *s;
+    if (v != 0) atomicCAS(&g_device_status, 0, v);
+}
+
+void enqueue_status_fold(int *status, cudaStream_t stream) { status_fold_kernel<<<1, 1, 0, stream>>>(status); }
+
+int read_and_clear_device_status(int *out) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return KDT_ECUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return KDT_ECUDA;
+    *out = v;
+    return KDT_OK;
+}
+
+// ---- per-kernel timing -------------------------------------------------------
+
+namespace {
+struct Pending {
+    const char *name;
+    cudaEvent_t ev0, ev1;
+    double bytes;
+};
+struct Total {
+    const char *name;
+    int64_t launches;
+    double ms;
+    double bytes;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<Pending> g_pending;
+std::vector<Total> g_totals;
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t s, const char *n, double b) : stream(s), name(n), bytes(b), ev0(nullptr), on(false) {
+    bool enabled;
+    {
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        enabled = g_prof_on;
+    }
+    if (!enabled) return;
+    if (cudaEventCreate(&ev0) != cudaSuccess) return;
+    cudaEventRecord(ev0, stream);
+    on = true;
+}
+
+ProfScope::~ProfScope() {
+    if (!on) return;
+    cudaEvent_t ev1;
+    if (cudaEventCreate(&ev1) != cudaSuccess) {
+        cudaEventDestroy(ev0);
+        return;
+    }
+    cudaEventRecord(ev1, stream);
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    g_pending.push_back({name, ev0, ev1, bytes});
+}
+
+static void drain_pending_locked() {
+    for (auto &p : g_pending) {
+        float ms = 0.f;
+        cudaEventSynchronize(p.ev1);
+        cudaEventElapsedTime(&ms, p.ev0, p.ev1);
+        cudaEventDestroy(p.ev0);
+        cudaEventDestroy(p.ev1);
+        bool found = false;
+        for (auto &t : g_totals) {
+            if (std::strcmp(t.name, p.name) == 0) {
+                t.launches += 1;
+                t.ms += ms;
+                t.bytes += p.bytes;
+                found = true;
+                break;
+            }
+        }
+        if (!found) g_totals.push_back({p.name, 1, (double)ms, p.bytes});
+    }
+    g_pending.clear();
+}
+
+}  // namespace kdt
+
+using namespace kdt;
+
+static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+extern "C" {
+
+int kdt_workspace_size(int64_t N, int k, int split_mode, size_t *bytes) {
+    if (!bytes) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    *bytes = p.bytes;
+    return KDT_OK;
+}
+
+int kdt_build_ws(const float *pts, int64_t N, int k, int split_mode, int32_t *perm, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    if (!pts || !perm || !workspace) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    if (workspace_bytes < p.bytes) return KDT_ENOMEM;
+    if (!aligned256(workspace)) return KDT_EINVAL;
+    return enqueue_build(p, carve(p, workspace), pts, perm, static_cast<cudaStream_t>(stream));
+}
+
+int kdt_build(const float *pts, int64_t N, int k, int split_mode, int32_t *perm, void *stream) {
+    if (!pts || !perm) return KDT_EINVAL;
+    Plan p;
+    int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, p.bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return KDT_ENOMEM;
+    }
+    rc = enqueue_build(p, carve(p, ws), pts, perm, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == KDT_OK) rc = KDT_ECUDA;
+    return rc;
+}
+
+int kdt_host_workspace_size(int64_t N, int k, int split_mode, size_t *bytes) {
+    if (!bytes) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    const size_t pts_bytes = ((size_t)N * k * 4 + 255) / 256 * 256;
+    const size_t perm_bytes = ((size_t)N * 4 + 255) / 256 * 256;
+    *bytes = p.bytes + pts_bytes + perm_bytes;
+    return KDT_OK;
+}
+
+int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode, int32_t *host_perm, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    if (!host_pts || !host_perm || !workspace) return KDT_EINVAL;
+    Plan p;
+    int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    size_t need = 0;
+    kdt_host_workspace_size(N, k, split_mode, &need);
+    if (workspace_bytes < need) return KDT_ENOMEM;
+    if (!aligned256(workspace)) return KDT_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *base = static_cast<unsigned char *>(workspace);
+    float *d_pts = reinterpret_cast<float *>(base + p.bytes);
+    int32_t *d_perm = reinterpret_cast<int32_t *>(base + p.bytes + ((size_t)N * k * 4 + 255) / 256 * 256);
+    const Buffers b = carve(p, workspace);
+    if (cudaMemcpyAsync(d_pts, host_pts, (size_t)N * k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return KDT_ECUDA;
+    rc = enqueue_build(p, b, d_pts, d_perm, s);
+    if (rc != KDT_OK) return rc;
+    if (cudaMemcpyAsync(host_perm, d_perm, (size_t)N * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDT_ECUDA;
+    int st = 0;
+    if (cudaMemcpyAsync(&st, b.status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KDT_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDT_ECUDA;
+    return st;
+}
+
+int kdt_verify(const float *pts, int64_t N, int k, int split_mode, const int32_t *perm, void *stream) {
+    if (!pts || !perm || N < 1 || N > 2147483647LL || k < 1 || k > kMaxK ||
+        (split_mode != KDT_SPLIT_ROUND_ROBIN && split_mode != KDT_SPLIT_WIDEST))
+        return KDT_EINVAL;
+    int result = 0;
+    const int rc = enqueue_verify(pts, N, k, split_mode, perm, static_cast<cudaStream_t>(stream), &result);
+    if (rc != KDT_OK) return rc;
+    return result;
+}
+
+int kdt_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDT_ECUDA;
+    int v = 0;
+    const int rc = read_and_clear_device_status(&v);
+    return rc != KDT_OK ? rc : v;
+}
+
+const char *kdt_error_string(int code) {
+    switch (code) {
+        case KDT_OK: return "ok";
+        case KDT_EINVAL: return "invalid argument";
+        case KDT_ENOMEM: return "out of memory or workspace too small";
+        case KDT_ECUDA: return "CUDA runtime error";
+        case KDT_ENONFINITE: return "non-finite coordinate";
+        case KDT_ETIMEOUT: return "device-side wait timed out";
+        case KDT_EINTERNAL: return "internal consistency check failed";
+        default: return "unknown error";
+    }
+}
+
+int kdt_profile_enable(int on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    g_prof_on = on != 0;
+    return KDT_OK;
+}
+
+int kdt_profile_reset(void) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    drain_pending_locked();
+    g_totals.clear();
+    return KDT_OK;
+}
+
+int kdt_profile_read(kdt_kernel_stat *out, int cap) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    drain_pending_locked();
+    const int n = (int)g_totals.size();
+    for (int i = 0; i < n && i < cap && out; ++i) {
+        out[i].name = g_totals[i].name;
+        out[i].launches = g_totals[i].launches;
+        out[i].total_ms = g_totals[i].ms;
+        out[i].bytes_alg = g_totals[i].bytes;
+    }
+    return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+// kdt_internal.cuh -- private declarations of the GB300 k-d tree builder.
+//
+// Notation ("GPU-friendly, Parallel, and (Almost-)In-Place Construction of
+// Left-Balanced k-d Trees", notation paragraph): nodes are numbered in level
+// order, level(i) = floor(log2(i+1)), L = numLevels(N) = level(N-1)+1,
+// F(l) = 2^l - 1 nodes above level l.  The paper announces O(1) forms for the
+// subtree size ss(s) and the segment begin sb(s,l) but its text does not
+// carry them; the forms below are derived from the left-balanced shape
+// (levels 0..L-2 full, level L-1 filled from the left with M = N - F(L-1)
+// nodes):
+//   for s on level l, j = s - F(l), B = 2^(L-1-l), A = B - 1:
+//     ss(s)   = A + clamp(M - j*B, 0, B)                (0 if s >= N)
+//     sb(s,l) = F(l) + j*A + min(M, j*B)
+// sb is the first array position of subtree s's points after level l has been
+// split off: the F(l) nodes already fixed occupy positions 0..F(l)-1 and the
+// live subtrees follow in node order.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kdtree_build.h"
+
+namespace kdt {
+
+constexpr int kMaxK = KDT_MAX_K;
+constexpr int kMaxWords = kMaxK + 1;  // k coordinate keys + the input index
+
+// ---- integer helpers usable on host and device -----------------------------
+
+__host__ __device__ __forceinline__ int ilog2_u64(uint64_t v) {
+#ifdef __CUDA_ARCH__
+    return 63 - __clzll((long long)v);
+#else
+    return 63 - __builtin_clzll(v);
+#endif
+}
+
+__host__ __device__ __forceinline__ int level_of(int64_t i) { return ilog2_u64((uint64_t)i + 1u); }
+
+__host__ __device__ __forceinline__ int64_t full_nodes(int l) { return ((int64_t)1 << l) - 1; }
+
+struct Shape {
+    int64_t N;  // number of points / nodes
+    int L;      // numLevels(N)
+    int64_t M;  // nodes on the last level
+};
+
+__host__ __device__ __forceinline__ Shape make_shape(int64_t N) {
+    Shape S;
+    S.N = N;
+    S.L = level_of(N - 1) + 1;
+    S.M = N - full_nodes(S.L - 1);
+    return S;
+}
+
+// ss(s) for node s on level l (0 if the node does not exist).
+__host__ __device__ __forceinline__ int64_t seg_size(const Shape &S, int l, int64_t s) {
+    if (l >= S.L || s >= S.N) return 0;
+    const int64_t B = (int64_t)1 << (S.L - 1 - l);
+    const int64_t A = B - 1;
+    const int64_t j = s - full_nodes(l);
+    int64_t r = S.M - j * B;
+    r = r < 0 ? 0 : (r > B ? B : r);
+    return A + r;
+}
+
+// sb(s, l) for node s on level l.
+__host__ __device__ __forceinline__ int64_t seg_begin(const Shape &S, int l, int64_t s) {
+    const int64_t B = (int64_t)1 << (S.L - 1 - l);
+    const int64_t A = B - 1;
+    const int64_t j = s - full_nodes(l);
+    const int64_t t = j * B;
+    return full_nodes(l) + j * A + (t < S.M ? t : S.M);
+}
+
+// Number of nodes that exist on level l.
+__host__ __device__ __forceinline__ int64_t nodes_on_level(const Shape &S, int l) {
+    const int64_t w = (int64_t)1 << l;
+    const int64_t left = S.N - full_nodes(l);
+    return left < w ? left : w;
+}
+
+// ---- order-preserving float keys -------------------------------------------
+// Unsigned comparison of the keys equals IEEE '<' on finite floats, with -0
+// folded onto +0 so that the two zeros compare equal (as '<' does).
+
+__device__ __forceinline__ uint32_t f2key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key2f(uint32_t k) {
+    const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+// Widest extent of a domain: argmax of hi - lo (float32, round to nearest),
+// lowest dimension on ties.
+__device__ __forceinline__ int widest_dim(const float *lo, const float *hi, int k) {
+    int best = 0;
+    float ext = __fsub_rn(hi[0], lo[0]);
+    for (int d = 1; d < k; ++d) {
+        const float e = __fsub_rn(hi[d], lo[d]);
+        if (e > ext) {
+            ext = e;
+            best = d;
+        }
+    }
+    return best;
+}
+
+// ---- device status ----------------------------------------------------------
+
+__device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
+
+// ---- workspace --------------------------------------------------------------
+
+// Finisher tile limits: a subtree whose point count is at most `tile` is
+// finished inside one CTA's shared memory.
+struct TilePlan {
+    int tile;          // T: max points per finisher CTA
+    size_t smem;       // dynamic shared memory per finisher CTA
+};
+
+struct Plan {
+    Shape S;
+    int k;
+    int mode;
+    int finish_level;    // first level whose largest segment fits a tile
+    TilePlan tp;
+    int64_t table_cap;   // node-table entries per level (mode 1)
+    // byte offsets inside the workspace
+    size_t off_status, off_bbox, off_keys[2], off_idx[2], off_dom[2], off_dim[2];
+    size_t bytes;
+};
+
+int make_plan(int64_t N, int k, int mode, Plan *p);
+
+struct Buffers {
+    int *status;
+    uint32_t *bbox;  // [2k]: min keys then max keys
+    uint32_t *keys[2];
+    uint32_t *idx[2];
+    float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
+    int *dim[2];
+};
+
+Buffers carve(const Plan &p, void *base);
+
+// Enqueues the whole build on `stream`.  Returns a KDT_* code for launch errors.
+int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *perm,
+                  cudaStream_t stream);
+
+// Per-kernel timing (profiling switch in kdt_api.cu).
+struct ProfScope {
+    cudaStream_t stream;
+    const char *name;
+    double bytes;
+    cudaEvent_t ev0;
+    bool on;
+    ProfScope(cudaStream_t s, const char *n, double b);
+    ~ProfScope();
+};
+
+// Folds a build's status word into the per-device status word.
+void enqueue_status_fold(int *status, cudaStream_t stream);
+int read_and_clear_device_status(int *out);
+
+int enqueue_verify(const float *pts, int64_t N, int k, int mode, const int32_t *perm,
+                   cudaStream_t stream, int *result);
+
+}  // namespace kdt

@@ -1,0 +1,366 @@
+#!/usr/bin/env python3
+"""Benchmark: left-balanced k-d tree build throughput on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload uniform_100m] [--no-e2e] [--no-cpu-baseline]
+
+One step = one complete build (every level of the method) of the workload's
+points, resident in HBM, through the C ABI with a caller-provided workspace.
+Prints ONE JSON line on rank 0.
+
+Multi-GPU (torchrun, one rank per GPU): the build does not shard, so every
+rank builds its own replica of the workload ("replicas only"); value = total
+points built by all ranks / max over ranks of the timed region.
+
+--impl reference times the CPU oracle (the plain single-threaded recursive
+builder) on the host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "points/sec for balanced k-d tree build (1×GB300) and % of HBM roofline"
+UNIT = "points/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return False
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return True
+
+
+def barrier(active: bool):
+    if active:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, active: bool, device=None) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if not active:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_identifier(dev_index: int) -> str | None:
+    try:
+        import torch
+        props = torch.cuda.get_device_properties(dev_index)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            s = str(uuid)
+            return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def b_alg(n: int) -> float:
+    """Algorithmic bytes of the level-by-level method: per point and sort
+    level 20 B (read tag, index and split coordinate; write tag and index),
+    plus 12 B per point for the final level-order gather."""
+    L = n.bit_length()  # numLevels(n) = floor(log2 n) + 1
+    return float(n) * (20.0 * (L - 1) + 12.0)
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+
+def cpu_baseline(workload, budget_s: float = 12.0) -> dict:
+    import oracle
+    o = oracle.get()
+    sample_n = 1 << 18
+    pts = workload.points(sample_n)
+    t0 = time.perf_counter()
+    o.build_tree(pts, workload.mode)
+    dt = time.perf_counter() - t0
+    reps = 1
+    # grow the sample towards the time budget (roughly 10-30 s of CPU work)
+    while dt * 4 < budget_s and sample_n < (1 << 22) and sample_n < workload.n:
+        sample_n *= 4
+        pts = workload.points(sample_n)
+        t0 = time.perf_counter()
+        o.build_tree(pts, workload.mode)
+        dt = time.perf_counter() - t0
+    return {"value": sample_n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{sample_n} points drawn from the {workload.name} distribution "
+                      f"(k={workload.k}, mode={workload.mode}), one full build, {reps} run, "
+                      f"single-threaded C oracle"}
+
+
+def run_reference(args, workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    o = oracle.get()
+    sample_n = args.ref_sample
+    pts = workload.points(sample_n)
+    for _ in range(args.warmup):
+        o.build_tree(pts, workload.mode)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.build_tree(pts, workload.mode)
+    dt = time.perf_counter() - t0
+    value = sample_n * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(workload, extra={"reference_sample_points": sample_n}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{sample_n} points of the {workload.name} distribution per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, extra=None) -> dict:
+    cfg = {"workload": w.name, "N": w.n, "k": w.k,
+           "split_mode": "round_robin" if w.mode == 0 else "widest",
+           "distribution": w.dist, "seed": w.seed, "layout": "AoS float32 in, int32 level-order perm out",
+           "l2": "no flush: inputs and workspace exceed the 129 MB L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# our build
+
+def run_ours(args, workload):
+    import torch
+    import balanced_tree_build_gb300 as kdt
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    active = init_dist(world, "nccl" if world > 1 else "gloo")
+    dev = torch.device("cuda", local)
+
+    pts_host = workload.points()
+    n, k = pts_host.shape
+    pts = torch.from_numpy(pts_host).to(dev)
+    perm = torch.empty(n, dtype=torch.int32, device=dev)
+    ws = kdt.alloc_workspace(n, k, workload.mode, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kdt.build_tree(pts, workload.mode, out=perm, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    rc = kdt.status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after warm-up: {rc}")
+
+    sampler = ClockSampler(gpu_identifier(local))
+    kdt.profile_reset()
+    kdt.profile_enable(True)
+    barrier(active)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(active)
+    clocks = sampler.stop()
+    kdt.profile_enable(False)
+    stats = kdt.profile_read()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, active, dev if active else None)
+    rc = kdt.status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after timed steps: {rc}")
+
+    total_points = float(n) * args.steps * world
+    value = total_points / (ms_max / 1e3)
+    ms_step = ms_max / args.steps
+
+    peak, peak_src = measured_peaks()
+    launches = sum(s["launches"] for s in stats)
+    dom = max(stats, key=lambda s: s["total_ms"]) if stats else None
+    roofline = None
+    if dom:
+        avg_ms = dom["total_ms"] / dom["launches"]
+        avg_bytes = dom["bytes_alg"] / dom["launches"]
+        achieved = avg_bytes / (avg_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                    "traffic": None, "avg_launch_ms": avg_ms, "alg_bytes_per_launch": avg_bytes}
+    balg = b_alg(n)
+    build_gbs = balg / (ms_step / 1e3) / 1e9
+    build_roof = {"B_alg_bytes": balg, "achieved_GBps": build_gbs, "frac_of_measured": build_gbs / peak,
+                  "frac_of_nominal_8TBps": build_gbs / NOMINAL_HBM_GBS}
+
+    e2e = None
+    if not args.no_e2e:
+        pin_pts = torch.from_numpy(pts_host).pin_memory()
+        pin_out = torch.empty(n, dtype=torch.int32).pin_memory()
+        hws = kdt.alloc_workspace(n, k, workload.mode, device=dev, host=True)
+        for _ in range(2):
+            kdt.build_tree_host(pin_pts, workload.mode, out=pin_out, workspace=hws, stream=stream)
+        e_steps = max(1, min(args.steps, 5))
+        barrier(active)
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            kdt.build_tree_host(pin_pts, workload.mode, out=pin_out, workspace=hws, stream=stream)
+        dt = time.perf_counter() - t0
+        dt = max_over_ranks(dt, active, dev if active else None)
+        e2e = {"value": float(n) * e_steps * world / dt, "unit": UNIT,
+               "h2d_bytes_per_step": int(n * k * 4), "d2h_bytes_per_step": int(n * 4),
+               "steps": e_steps, "api": "kdt_build_host (pinned host buffers)"}
+        del hws
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(workload)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(workload, extra={"parallelism": f"replicas x{world}"}),
+            "roofline": roofline, "build_roofline": build_roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "kernels": stats, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if active:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="uniform_100m")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample", type=int, default=1 << 18,
+                    help="points per step for --impl reference")
+    args = ap.parse_args(argv)
+    from balanced_tree_build_gb300.inputs import WORKLOADS
+    workload = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, workload)
+    return run_ours(args, workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,142 @@
+/*
+ * kdtree_build.h -- C ABI of the GB300 left-balanced k-d tree builder.
+ *
+ * Builds the left-balanced, complete k-d tree over N points of k float32
+ * coordinates, stored implicitly in level order: node 0 is the root, node i
+ * has children 2i+1 and 2i+2 and parent (i-1)/2 ("GPU-friendly, Parallel, and
+ * (Almost-)In-Place Construction of Left-Balanced k-d Trees", notation
+ * paragraph).  Every node satisfies the k-d condition of that paper's problem
+ * paragraph -- its left subtree lies on the low side and its right subtree on
+ * the high side of its split plane -- and the tree's shape is the
+ * left-balanced complete shape, which fixes every subtree's size.
+ *
+ * Ordering.  Points are compared in split dimension p by the strict total
+ * order (x[p], x[p+1 mod k], ..., x[p-1 mod k], input index): the cyclic
+ * "super key" of "An Implementation of a Balanced Kd Tree Builder Using GPUs"
+ * (sort paragraph), with the input index as the final tiebreak.  Coordinates
+ * compare as IEEE floats (-0 equals +0).  Under this order the tree is
+ * unique, so results are reproducible bit for bit.
+ *
+ * Split rule (split_mode):
+ *   KDT_SPLIT_ROUND_ROBIN (0): dimension level(node) mod k (round-robin
+ *       paragraph of the left-balanced paper);
+ *   KDT_SPLIT_WIDEST (1): the dimension of widest extent of the node's domain,
+ *       lowest dimension on ties; the root's domain is the bounding box of all
+ *       points and each child's domain is its parent's cut at the parent's
+ *       split coordinate (split-widest-dimension paragraphs of the same
+ *       paper).  Extents are float32 differences hi - lo.
+ *
+ * Output.  perm[node] = input index of the point stored at level-order node
+ * `node` (so the points of the tree are pts[perm[0]], pts[perm[1]], ...).
+ *
+ * Layouts.  pts is row-major N x k float32 (k adjacent coordinates per point,
+ * the "coordinate array" layout of the KdTreeGPU page); perm is int32[N].
+ * Limits: 1 <= N <= 2^31 - 1, 1 <= k <= KDT_MAX_K.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Calls marked "stream-ordered" only enqueue work and return;
+ * the caller synchronises before reading results.  Calls marked "synchronous"
+ * return after the work is complete.
+ *
+ * Errors.  Every call returns a KDT_* code.  Argument errors are detected on
+ * the host and returned at once, before anything is enqueued.  Errors found on
+ * the device (non-finite input, an internal consistency check) are recorded in
+ * a per-device status word that kdt_status() returns and clears; the
+ * synchronous calls return them directly.  After a device-side error the
+ * contents of perm are unspecified.
+ *
+ * Thread safety.  Calls on different streams may overlap when each uses its
+ * own workspace.  The per-device status word is shared by all builds in the
+ * process.
+ */
+#ifndef KDTREE_BUILD_H
+#define KDTREE_BUILD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDT_OK 0
+#define KDT_EINVAL (-1)     /* bad argument (null pointer, N, k, mode, size) */
+#define KDT_ENOMEM (-2)     /* device allocation failed, or workspace too small */
+#define KDT_ECUDA (-3)      /* a CUDA runtime call failed */
+#define KDT_ENONFINITE (-4) /* a coordinate is NaN or infinite */
+#define KDT_ETIMEOUT (-5)   /* a bounded device-side wait gave up */
+#define KDT_EINTERNAL (-6)  /* a device-side consistency check failed */
+
+#define KDT_SPLIT_ROUND_ROBIN 0
+#define KDT_SPLIT_WIDEST 1
+
+#define KDT_MAX_K 16
+
+/* Bytes of device scratch that a build of (N, k, split_mode) needs.
+ * Host-only; returns KDT_EINVAL for arguments kdt_build would reject. */
+int kdt_workspace_size(int64_t N, int k, int split_mode, size_t *bytes);
+
+/* Builds the tree.  pts (read-only) and perm (fully overwritten) are DEVICE
+ * pointers owned by the caller.  Scratch memory is allocated and freed
+ * stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ * Stream-ordered. */
+int kdt_build(const float *pts, int64_t N, int k, int split_mode,
+              int32_t *perm, void *stream);
+
+/* Same as kdt_build with caller-provided device scratch: `workspace` must hold
+ * at least kdt_workspace_size() bytes, be 256-byte aligned and must not be in
+ * use by another call until this build completes on `stream`.  Allocates
+ * nothing.  Stream-ordered. */
+int kdt_build_ws(const float *pts, int64_t N, int k, int split_mode,
+                 int32_t *perm, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/* Host-buffer variant: host_pts and host_perm are HOST pointers (pinned memory
+ * gives asynchronous copies; pageable memory works but is staged by CUDA).
+ * Device scratch is `workspace` (at least kdt_host_workspace_size() bytes),
+ * which also receives the copied points and the device-side permutation.
+ * Copies the points to the device, builds, copies the permutation back.
+ * Synchronous; returns device-side errors directly. */
+int kdt_host_workspace_size(int64_t N, int k, int split_mode, size_t *bytes);
+int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode,
+                   int32_t *host_perm, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Checks that perm (DEVICE pointer) is the tree of pts: perm is a permutation
+ * of 0..N-1 and every node satisfies the k-d condition against every one of
+ * its ancestors under the order and split rule above (the verifier idea of
+ * the KdTreeGPU page).  Because the tree is unique, "valid" is equivalent to
+ * "equal to the reference result".  Allocates its scratch stream-ordered.
+ * Synchronous: returns 0 if valid, 1 if not, or a negative KDT_* code. */
+int kdt_verify(const float *pts, int64_t N, int k, int split_mode,
+               const int32_t *perm, void *stream);
+
+/* Synchronises `stream`, then returns and clears the calling thread's current
+ * device's status word (KDT_OK if no device-side error was recorded). */
+int kdt_status(void *stream);
+
+/* Human-readable name of a KDT_* code (static string). */
+const char *kdt_error_string(int code);
+
+/* Per-kernel timing.  When enabled, the build records CUDA events around each
+ * of its kernel launches (on the build's stream) and accumulates, per kernel
+ * family, the launch count and total device time.  kdt_profile_read fills up
+ * to `cap` entries (names are static strings) and returns the number of
+ * families; it synchronises on the events it reads.  kdt_profile_reset clears
+ * the totals.  Off by default. */
+typedef struct {
+    const char *name;
+    int64_t launches;
+    double total_ms;
+    double bytes_alg; /* algorithmic bytes summed over the launches */
+} kdt_kernel_stat;
+
+int kdt_profile_enable(int on);
+int kdt_profile_reset(void);
+int kdt_profile_read(kdt_kernel_stat *out, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDTREE_BUILD_H */
