@@ -331,20 +331,27 @@ __device__ __forceinline__ int fin_dim(const FinArgs &a, const FinSmem &sm, int6
 // Fixes node u (level j) inside one warp: selects its split point among the
 // n_u points at ids[cur][off_u..], writes perm[u], and moves the other local
 // ids to the children's ranges of ids[cur^1].
-__device__ void warp_split_node(const FinArgs &a, const FinSmem &sm, int64_t s0, int j, int64_t u,
-                                int cur, uint32_t *wf, uint32_t *hist) {
+//
+// The warp owns the subtree of node t (level jt) whose points occupied
+// [off_t, off_t + n_t) when the warp took it over.  Offsets below are laid out
+// relative to that range, which therefore never moves: the descendants of t
+// on each level are packed from off_t.  (Laid out relative to the whole tile
+// instead, the ranges would shift left as medians leave, into a range that a
+// neighbouring, unsynchronised warp may still be reading.)
+__device__ void warp_split_node(const FinArgs &a, const FinSmem &sm, int64_t s0, int64_t t, int jt,
+                                uint32_t off_t, int j, int64_t u, int cur, uint32_t *wf, uint32_t *hist) {
     const uint32_t lane = threadIdx.x & 31u;
     const Shape &S = a.S;
     const int depth = j - a.l0;
-    const int64_t tile_base_j = seg_begin(S, j, ((s0 + 1) << depth) - 1);
+    const int64_t sub_base_j = seg_begin(S, j, ((t + 1) << (j - jt)) - 1);
     const uint32_t n_u = (uint32_t)seg_size(S, j, u);
-    const uint32_t off_u = (uint32_t)(seg_begin(S, j, u) - tile_base_j);
+    const uint32_t off_u = off_t + (uint32_t)(seg_begin(S, j, u) - sub_base_j);
     const bool has_children = j + 1 < S.L;
     const uint32_t m_u = has_children ? (uint32_t)seg_size(S, j + 1, 2 * u + 1) : 0u;
     uint32_t left_off = 0;
     if (has_children) {
-        const int64_t tile_base_j1 = seg_begin(S, j + 1, ((s0 + 1) << (depth + 1)) - 1);
-        left_off = (uint32_t)(seg_begin(S, j + 1, 2 * u + 1) - tile_base_j1);
+        const int64_t sub_base_j1 = seg_begin(S, j + 1, ((t + 1) << (j + 1 - jt)) - 1);
+        left_off = off_t + (uint32_t)(seg_begin(S, j + 1, 2 * u + 1) - sub_base_j1);
     }
     const uint32_t right_off = left_off + m_u;
     const int d = fin_dim(a, sm, s0, j, u);
@@ -555,9 +562,11 @@ __global__ void __launch_bounds__(kFinThreads) finisher_kernel(FinArgs a) {
         const int64_t count0 = (int64_t)1 << depth0;
         uint32_t *hist = sm.hist + w * kWarpRadixBins;
         uint32_t *wf = wfs[w];
+        const int64_t tile_base = seg_begin(S, j, first0);
         for (int64_t o = w; o < count0; o += kFinWarps) {
             const int64_t t = first0 + o;
             if (t >= N) break;
+            const uint32_t off_t = (uint32_t)(seg_begin(S, j, t) - tile_base);
             int c = cur;
             for (int jj = j; jj < S.L; ++jj, c ^= 1) {
                 const int dd = jj - j;
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kFinThreads) finisher_kernel(FinArgs a) {
                 for (int64_t oo = 0; oo < cnt; ++oo) {
                     const int64_t u = f + oo;
                     if (u >= N) break;
-                    warp_split_node(a, sm, s0, jj, u, c, wf, hist);
+                    warp_split_node(a, sm, s0, t, j, off_t, jj, u, c, wf, hist);
                 }
                 __syncwarp();
             }

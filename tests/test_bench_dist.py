@@ -1,0 +1,54 @@
+"""Host logic of bench.py's multi-rank (replica) path on CPU with gloo, and
+the algorithmic-bytes model (no GPU)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    w, r, _ = bench.dist_env()
+    active = bench.init_dist(w, "gloo")
+    bench.barrier(active)
+    got = bench.max_over_ranks(10.0 + 5.0 * r, active)
+    q.put((r, got))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_single_rank_is_passthrough():
+    assert bench.max_over_ranks(3.5, False) == 3.5
+
+
+def test_b_alg_model():
+    # N = 10: L = 4 levels, 3 sort levels
+    assert bench.b_alg(10) == 10 * (20 * 3 + 12)
+    assert bench.b_alg(100_000_000) == pytest.approx(53.2e9, rel=1e-3)
+    assert bench.b_alg(1) == 12.0
