@@ -135,6 +135,36 @@ int kdt_profile_enable(int on);
 int kdt_profile_reset(void);
 int kdt_profile_read(kdt_kernel_stat *out, int cap);
 
+/* Build without any device allocation, for callers that cannot allocate.
+ * The paper has no counterpart to this entry point; it is a library convenience.
+ *
+ * Some callers are not allowed to call cudaMalloc or cudaMallocAsync at the
+ * point where they build a tree: a plugin whose host application owns every
+ * byte of device memory through its own pool, a latency-critical loop where
+ * an allocation could synchronise the device or fail under memory pressure,
+ * or a caller that simply has no allocator to hand.  This entry point takes
+ * the same inputs and output as kdt_build but uses, as its scratch, one
+ * fixed array of KDT_STATIC_SCRATCH_BYTES bytes that the library reserves on
+ * every device that loads it (held until the process exits).
+ *
+ * Limit: the build must fit the array, i.e. kdt_workspace_size(N, k,
+ * split_mode) <= KDT_STATIC_SCRATCH_BYTES (about 0.5-1 million points for
+ * k = 3); larger builds are rejected with KDT_EINVAL before anything is
+ * enqueued.  Other argument errors also return KDT_EINVAL.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream
+ * capture.  Every call clears the parts of the array that must start at
+ * zero, so one call's leftovers never affect the next.  All calls share the
+ * one array: calls whose work overlaps on the GPU (for example on two
+ * streams without ordering between them) race and corrupt each other's
+ * results; order them on one stream or with events.
+ *
+ * pts and perm are DEVICE pointers as for kdt_build.  Stream-ordered. */
+#define KDT_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int kdt_build_static(const float *pts, int64_t N, int k, int split_mode,
+                     int32_t *perm, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
