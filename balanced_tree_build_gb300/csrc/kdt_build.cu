@@ -27,7 +27,6 @@
 namespace kdt {
 
 constexpr int kInitThreads = 256;
-constexpr int kSegThreads = 512;
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kWarpMax = 256;          // finisher: subtrees this small go to one warp
@@ -37,7 +36,7 @@ constexpr size_t kFinSmemBudget = 200 * 1024;
 // init: AoS float points -> SoA keys + index; finiteness; bounding box
 
 __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restrict__ pts, int64_t N,
-                                                            int k, int mode, uint32_t *__restrict__ keys,
+                                                            int k, uint32_t *__restrict__ keys,
                                                             uint32_t *__restrict__ idx,
                                                             uint32_t *__restrict__ bbox,
                                                             int *__restrict__ status) {
@@ -64,22 +63,20 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
         idx[i] = (uint32_t)i;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
-    if (mode == KDT_SPLIT_WIDEST) {
 #pragma unroll
-        for (int c = 0; c < kMaxK; ++c) {
-            if (c < k) {
-                const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
-                const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
-                if ((threadIdx.x & 31) == 0) {
-                    atomicMin(&bbox[c], a);
-                    atomicMax(&bbox[k + c], b);
-                }
+    for (int c = 0; c < kMaxK; ++c) {
+        if (c < k) {
+            const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
+            const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
+            if ((threadIdx.x & 31) == 0) {
+                atomicMin(&bbox[c], a);
+                atomicMax(&bbox[k + c], b);
             }
         }
     }
 }
 
-// Root node table entry (widest mode): domain = bounding box, dim = widest.
+// Root node table entry: domain = bounding box of all points, dim = widest.
 __global__ void root_table_kernel(const uint32_t *bbox, int k, float *dom, int *dim) {
     float lo[kMaxK], hi[kMaxK];
     for (int c = 0; c < k; ++c) {
@@ -89,147 +86,6 @@ __global__ void root_table_kernel(const uint32_t *bbox, int k, float *dom, int *
         dom[k + c] = hi[c];
     }
     dim[0] = widest_dim(lo, hi, k);
-}
-
-// ---------------------------------------------------------------------------
-// level split of one subtree per CTA (records in global memory)
-
-struct SegArgs {
-    Shape S;
-    int k, mode, l;
-    const uint32_t *src_keys, *src_idx;
-    uint32_t *dst_keys, *dst_idx;
-    int32_t *perm;
-    const float *dom_cur;
-    const int *dim_cur;
-    float *dom_nxt;
-    int *dim_nxt;
-    int *status;
-};
-
-// Word i of the point at offset q of a subtree whose records start at `base`.
-struct GlobalSeg {
-    const uint32_t *keys, *idx;
-    int64_t N, base;
-    int k, d;
-    __device__ __forceinline__ uint32_t operator()(int i, uint32_t q) const {
-        if (i == k) return idx[base + q];
-        int c = d + i;
-        if (c >= k) c -= k;
-        return keys[(int64_t)c * N + base + q];
-    }
-};
-
-// Child domains for the widest-dimension rule: the parent's domain with the
-// split coordinate as the left child's upper bound and the right child's
-// lower bound (split-widest-dimension passage: clip by the split plane).
-__device__ void write_child_domains(const float *dom_p, int k, int d, float split, float *dom_l,
-                                    int *dim_l, float *dom_r, int *dim_r) {
-    float lo[kMaxK], hi[kMaxK];
-    for (int c = 0; c < k; ++c) {
-        lo[c] = dom_p[c];
-        hi[c] = dom_p[k + c];
-    }
-    const float h = hi[d];
-    hi[d] = split;
-    for (int c = 0; c < k; ++c) {
-        dom_l[c] = lo[c];
-        dom_l[k + c] = hi[c];
-    }
-    *dim_l = widest_dim(lo, hi, k);
-    hi[d] = h;
-    lo[d] = split;
-    for (int c = 0; c < k; ++c) {
-        dom_r[c] = lo[c];
-        dom_r[k + c] = hi[c];
-    }
-    *dim_r = widest_dim(lo, hi, k);
-}
-
-__global__ void __launch_bounds__(kSegThreads) level_seg_kernel(SegArgs a) {
-    __shared__ SelState st;
-    __shared__ uint32_t hist[kCtaRadixBins];
-    __shared__ uint32_t red[64];
-    __shared__ uint32_t medw[kMaxWords];
-    __shared__ uint32_t cursor[2];
-    __shared__ int stop;
-    const uint32_t tid = threadIdx.x;
-    if (tid == 0) stop = *(volatile int *)a.status;
-    __syncthreads();
-    if (stop) return;
-
-    const int64_t s = full_nodes(a.l) + blockIdx.x;
-    const uint32_t n = (uint32_t)seg_size(a.S, a.l, s);
-    const int64_t base = seg_begin(a.S, a.l, s);
-    const uint32_t m = (uint32_t)seg_size(a.S, a.l + 1, 2 * s + 1);
-    const int64_t jn = s - full_nodes(a.l);
-    const int d = a.mode == KDT_SPLIT_ROUND_ROBIN ? a.l % a.k : a.dim_cur[jn];
-    const GlobalSeg acc{a.src_keys, a.src_idx, a.S.N, base, a.k, d};
-
-    cta_select(acc, n, m, a.k + 1, st, hist, red);
-    if (st.err) {
-        if (tid == 0) set_status(a.status, KDT_EINTERNAL);
-        return;
-    }
-    if (tid <= (uint32_t)a.k) medw[tid] = acc((int)tid, st.med_q);
-    if (tid < 2) cursor[tid] = 0u;
-    __syncthreads();
-
-    const uint32_t nr = n - m - 1u;
-    const bool has_children = a.l + 1 < a.S.L;
-    const int64_t left_begin = has_children ? seg_begin(a.S, a.l + 1, 2 * s + 1) : 0;
-    const int64_t right_begin = left_begin + m;
-    const int64_t N = a.S.N;
-    const uint32_t lane = tid & 31u;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (uint32_t q0 = 0; q0 < n; q0 += blockDim.x) {
-        const uint32_t q = q0 + tid;
-        int side = -1;  // 0 = left, 1 = right, -1 = none / the median
-        if (q < n) {
-            const int c = cmp_words(acc, q, medw, a.k + 1);
-            side = c < 0 ? 0 : (c > 0 ? 1 : -1);
-        }
-        const uint32_t lm = __ballot_sync(0xffffffffu, side == 0);
-        const uint32_t rm = __ballot_sync(0xffffffffu, side == 1);
-        uint32_t lb = 0, rb = 0;
-        if (lane == 0) {
-            if (lm) lb = atomicAdd(&cursor[0], __popc(lm));
-            if (rm) rb = atomicAdd(&cursor[1], __popc(rm));
-        }
-        lb = __shfl_sync(0xffffffffu, lb, 0);
-        rb = __shfl_sync(0xffffffffu, rb, 0);
-        if (side >= 0) {
-            int64_t pos;
-            bool ok;
-            if (side == 0) {
-                const uint32_t o = lb + __popc(lm & lt_mask);
-                pos = left_begin + o;
-                ok = o < m;
-            } else {
-                const uint32_t o = rb + __popc(rm & lt_mask);
-                pos = right_begin + o;
-                ok = o < nr;
-            }
-            if (ok) {
-                for (int c = 0; c < a.k; ++c)
-                    a.dst_keys[(int64_t)c * N + pos] = a.src_keys[(int64_t)c * N + base + q];
-                a.dst_idx[pos] = a.src_idx[base + q];
-            } else {
-                set_status(a.status, KDT_EINTERNAL);
-            }
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        if (cursor[0] != m || cursor[1] != nr) set_status(a.status, KDT_EINTERNAL);
-        a.perm[s] = (int32_t)medw[a.k];
-        if (a.mode == KDT_SPLIT_WIDEST && has_children) {
-            const int k = a.k;
-            write_child_domains(a.dom_cur + jn * 2 * k, k, d, key2f(medw[0]),
-                                a.dom_nxt + (2 * jn) * 2 * k, a.dim_nxt + 2 * jn,
-                                a.dom_nxt + (2 * jn + 1) * 2 * k, a.dim_nxt + 2 * jn + 1);
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -611,24 +467,34 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     int lf = 0;
     while (lf < q.S.L && seg_size(q.S, lf, full_nodes(lf)) > q.tp.tile) ++lf;
     q.finish_level = lf;
-    q.table_cap = mode == KDT_SPLIT_WIDEST ? ((int64_t)1 << lf) : 0;
+    int lm = 0;
+    while (lm < lf && ((int64_t)1 << lm) <= kMultiMaxSegs && seg_size(q.S, lm, full_nodes(lm)) > kMultiMinSize) ++lm;
+    q.multi_levels = lm;
+    q.table_cap = (int64_t)1 << lf;
+    q.hist_rows = lm > 0 ? ((int64_t)1 << (lm - 1)) : 0;
+    q.sel_cap = lf > 0 ? ((int64_t)1 << (lf - 1)) : 0;
     size_t off = 0;
     q.off_status = off;
     off = align_up(off + 64, 256);
     q.off_bbox = off;
     off = align_up(off + (size_t)2 * k * 4, 256);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
+        const int64_t rows = (b < 2 || lf > 0) ? N : 0;
         q.off_keys[b] = off;
-        off = align_up(off + (size_t)k * N * 4, 256);
+        off = align_up(off + (size_t)k * rows * 4, 256);
         q.off_idx[b] = off;
-        off = align_up(off + (size_t)N * 4, 256);
+        off = align_up(off + (size_t)rows * 4, 256);
     }
     for (int b = 0; b < 2; ++b) {
         q.off_dom[b] = off;
         off = align_up(off + (size_t)q.table_cap * 2 * k * 4, 256);
         q.off_dim[b] = off;
         off = align_up(off + (size_t)q.table_cap * 4, 256);
+        q.off_hist[b] = off;
+        off = align_up(off + (size_t)q.hist_rows * kBuckets * 4, 256);
     }
+    q.off_sel = off;
+    off = align_up(off + (size_t)q.sel_cap * sizeof(SegSel), 256);
     q.bytes = off;
     *p = q;
     return KDT_OK;
@@ -639,12 +505,16 @@ Buffers carve(const Plan &p, void *base) {
     Buffers r;
     r.status = reinterpret_cast<int *>(b + p.off_status);
     r.bbox = reinterpret_cast<uint32_t *>(b + p.off_bbox);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
         r.keys[i] = reinterpret_cast<uint32_t *>(b + p.off_keys[i]);
         r.idx[i] = reinterpret_cast<uint32_t *>(b + p.off_idx[i]);
+    }
+    for (int i = 0; i < 2; ++i) {
         r.dom[i] = reinterpret_cast<float *>(b + p.off_dom[i]);
         r.dim[i] = reinterpret_cast<int *>(b + p.off_dim[i]);
+        r.hist[i] = reinterpret_cast<uint32_t *>(b + p.off_hist[i]);
     }
+    r.sel = reinterpret_cast<SegSel *>(b + p.off_sel);
     return r;
 }
 
@@ -659,10 +529,8 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
     const int k = p.k;
     const double Nd = (double)S.N;
     if (cudaMemsetAsync(b.status, 0, sizeof(int), stream) != cudaSuccess) return KDT_ECUDA;
-    if (p.mode == KDT_SPLIT_WIDEST) {
-        if (cudaMemsetAsync(b.bbox, 0xff, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
-        if (cudaMemsetAsync(b.bbox + k, 0x00, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
-    }
+    if (cudaMemsetAsync(b.bbox, 0xff, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
+    if (cudaMemsetAsync(b.bbox + k, 0x00, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
     {
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
@@ -670,36 +538,17 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         int64_t blocks = (S.N + kInitThreads - 1) / kInitThreads;
         const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;
         if (blocks > cap) blocks = cap;
-        ProfScope ps(stream, "init", Nd * (4.0 * k + 4.0 * k + 4.0));
-        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.mode, b.keys[0], b.idx[0],
-                                                                   b.bbox, b.status);
+        ProfScope ps(stream, "init", 0.0);
+        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, b.keys[0], b.idx[0], b.bbox,
+                                                                   b.status);
         KDT_LAUNCH_CHECK();
     }
-    if (p.mode == KDT_SPLIT_WIDEST) {
-        root_table_kernel<<<1, 1, 0, stream>>>(b.bbox, k, b.dom[0], b.dim[0]);
-        KDT_LAUNCH_CHECK();
-    }
+    root_table_kernel<<<1, 1, 0, stream>>>(b.bbox, k, b.dom[0], b.dim[0]);
+    KDT_LAUNCH_CHECK();
     int src = 0;
     for (int l = 0; l < p.finish_level; ++l) {
-        SegArgs a;
-        a.S = S;
-        a.k = k;
-        a.mode = p.mode;
-        a.l = l;
-        a.src_keys = b.keys[src];
-        a.src_idx = b.idx[src];
-        a.dst_keys = b.keys[src ^ 1];
-        a.dst_idx = b.idx[src ^ 1];
-        a.perm = perm;
-        a.dom_cur = b.dom[l & 1];
-        a.dim_cur = b.dim[l & 1];
-        a.dom_nxt = b.dom[(l + 1) & 1];
-        a.dim_nxt = b.dim[(l + 1) & 1];
-        a.status = b.status;
-        const int64_t nseg = nodes_on_level(S, l);
-        ProfScope ps(stream, "level_seg", 20.0 * Nd);
-        level_seg_kernel<<<(unsigned)nseg, kSegThreads, 0, stream>>>(a);
-        KDT_LAUNCH_CHECK();
+        const int rc = enqueue_level(p, b, l, src, perm, stream);
+        if (rc != KDT_OK) return rc;
         src ^= 1;
     }
     {

@@ -124,15 +124,29 @@ struct TilePlan {
     size_t smem;       // dynamic shared memory per finisher CTA
 };
 
+// Per live subtree of a global level: the value bucket that holds the split
+// rank, the point counts below it and in it, and the partition cursors.
+struct SegSel {
+    uint32_t bstar, below, cnt;
+    uint32_t curL, curC, curR;
+};
+
+constexpr int kBuckets = 2048;         // value buckets per subtree on global levels
+constexpr int kMultiMaxSegs = 1024;    // multi-CTA levels: at most this many subtrees ...
+constexpr int64_t kMultiMinSize = 65536;  // ... each larger than this
+
 struct Plan {
     Shape S;
     int k;
     int mode;
-    int finish_level;    // first level whose largest segment fits a tile
+    int finish_level;    // first level whose largest subtree fits a finisher tile
+    int multi_levels;    // levels [0, multi_levels) use the multi-CTA pipeline
     TilePlan tp;
-    int64_t table_cap;   // node-table entries per level (mode 1)
+    int64_t table_cap;   // node-table entries per level
+    int64_t hist_rows;   // histogram rows per buffer (multi-CTA levels)
+    int64_t sel_cap;     // SegSel entries
     // byte offsets inside the workspace
-    size_t off_status, off_bbox, off_keys[2], off_idx[2], off_dom[2], off_dim[2];
+    size_t off_status, off_bbox, off_keys[3], off_idx[3], off_dom[2], off_dim[2], off_hist[2], off_sel;
     size_t bytes;
 };
 
@@ -141,13 +155,18 @@ int make_plan(int64_t N, int k, int mode, Plan *p);
 struct Buffers {
     int *status;
     uint32_t *bbox;  // [2k]: min keys then max keys
-    uint32_t *keys[2];
-    uint32_t *idx[2];
+    uint32_t *keys[3];  // record buffers: [0], [1] ping-pong, [2] bucket candidates
+    uint32_t *idx[3];
     float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
     int *dim[2];
+    uint32_t *hist[2];  // [rows][kBuckets]
+    SegSel *sel;
 };
 
 Buffers carve(const Plan &p, void *base);
+
+// Enqueues one global level l (records move from buffer src to src^1).
+int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm, cudaStream_t stream);
 
 // Enqueues the whole build on `stream`.  Returns a KDT_* code for launch errors.
 int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *perm,

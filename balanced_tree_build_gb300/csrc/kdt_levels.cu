@@ -1,0 +1,633 @@
+// kdt_levels.cu -- the global levels of the build: one record pass per level.
+//
+// For every live subtree s of level l the method needs the point of rank
+// m = ss(lChild(s)) under s's split order, and the split of the other points
+// into lChild(s) and rChild(s) ("GPU-friendly, Parallel, and (Almost-)In-Place
+// Construction of Left-Balanced k-d Trees", core-idea and tag-update
+// passages).  Here that is done in three steps:
+//
+//  1. histogram: each point's split coordinate falls into one of kBuckets
+//     value buckets spread evenly over s's domain [lo, hi] in the split
+//     dimension (the bucket index is a monotone function of the coordinate);
+//  2. pick: the bucket b* that holds rank m, and the counts below it;
+//  3. partition: points in buckets below b* certainly go left, above b*
+//     certainly right; they are written straight to the children's ranges.
+//     Points in b* ("candidates", typically a few per thousand) go to a side
+//     buffer; an exact most-significant-digit select over the full split
+//     order (cyclic super key, then input index) among them fixes the split
+//     point and places the rest.
+//
+// Step 1 for level l+1 is fused into step 3 of level l when the next split
+// dimension differs from the current one (round-robin rule, k >= 2): the
+// child's domain in that dimension is the parent's, so the child's buckets
+// are known while the parent is partitioned.
+//
+// Large subtrees (few per level) are spread over all SMs ("multi-CTA"
+// pipeline: separate histogram / pick / partition / resolve kernels with
+// per-subtree cursors); once there are many smaller subtrees each CTA owns
+// one subtree and runs all steps itself ("seg" kernel).
+#include "kdt_internal.cuh"
+#include "kdt_select.cuh"
+
+namespace kdt {
+
+constexpr int kLvlThreads = 512;
+constexpr int kPickThreads = 256;
+constexpr int kEPT = 8;                          // points per thread per tile
+constexpr int kTile = kLvlThreads * kEPT;
+
+// ---- value buckets ----------------------------------------------------------
+
+struct Bucketer {
+    float lo, scale;
+    // Monotone non-decreasing in the coordinate: fsub and fmul round to
+    // nearest (monotone), truncation and clamping are monotone.
+    __device__ __forceinline__ int operator()(uint32_t key) const {
+        const float x = key2f(key);
+        const float t = __fmul_rn(__fsub_rn(x, lo), scale);
+        int b = __float2int_rz(t);
+        b = b < 0 ? 0 : b;
+        return b < kBuckets ? b : kBuckets - 1;
+    }
+};
+
+__device__ __forceinline__ Bucketer make_bucketer(float lo, float hi) {
+    const float r = __fsub_rn(hi, lo);
+    float scale = 0.f;  // empty or non-finite range: every point in bucket 0
+    if (r > 0.f && r <= 3.0e38f) {
+        scale = __fdiv_rn((float)kBuckets, r);
+        if (!(scale <= 3.0e38f)) scale = 0.f;
+    }
+    Bucketer b;
+    b.lo = lo;
+    b.scale = scale;
+    return b;
+}
+
+// Subtree of level l that holds array position p (inverse of sb).
+__device__ __forceinline__ int64_t seg_of_pos(const Shape &S, int l, int64_t p) {
+    const int64_t B = (int64_t)1 << (S.L - 1 - l), A = B - 1;
+    const int64_t q = p - full_nodes(l);
+    const int64_t nf = S.M / B;          // subtrees with a full last-level part
+    const int64_t r = S.M - nf * B;      // last-level part of subtree nf
+    const int64_t full_end = nf * (A + B);
+    int64_t j;
+    if (q < full_end) {
+        j = q / (A + B);
+    } else {
+        const int64_t q2 = q - full_end;
+        if (r > 0) j = q2 < A + r ? nf : nf + 1 + (q2 - (A + r)) / A;
+        else j = nf + q2 / A;
+    }
+    return full_nodes(l) + j;
+}
+
+// ---- per-level arguments -----------------------------------------------------
+
+struct LevelArgs {
+    Shape S;
+    int k, mode, l;
+    const uint32_t *src_keys, *src_idx;
+    uint32_t *dst_keys, *dst_idx;
+    uint32_t *cand_keys, *cand_idx;
+    int32_t *perm;
+    const float *dom_cur;
+    const int *dim_cur;
+    float *dom_nxt;
+    int *dim_nxt;
+    uint32_t *hist_cur;  // [subtrees][kBuckets] (multi-CTA levels)
+    uint32_t *hist_nxt;  // children's histograms (fused next level) or null
+    SegSel *sel;
+    int *status;
+    int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
+};
+
+struct SegInfo {
+    int64_t s, j, base, left_begin;
+    uint32_t n, m, nr;
+    int d;
+};
+
+__device__ __forceinline__ SegInfo seg_info(const LevelArgs &a, int64_t s) {
+    SegInfo g;
+    g.s = s;
+    g.j = s - full_nodes(a.l);
+    g.base = seg_begin(a.S, a.l, s);
+    g.n = (uint32_t)seg_size(a.S, a.l, s);
+    g.m = (uint32_t)seg_size(a.S, a.l + 1, 2 * s + 1);
+    g.nr = g.n - g.m - 1u;
+    g.left_begin = seg_begin(a.S, a.l + 1, 2 * s + 1);
+    g.d = a.mode == KDT_SPLIT_ROUND_ROBIN ? a.l % a.k : a.dim_cur[g.j];
+    return g;
+}
+
+__device__ __forceinline__ Bucketer seg_bucketer(const LevelArgs &a, int64_t j, int d) {
+    const float *dom = a.dom_cur + j * 2 * a.k;
+    return make_bucketer(dom[d], dom[a.k + d]);
+}
+
+__device__ __forceinline__ bool stop_requested(const int *status, int *flag) {
+    if (threadIdx.x == 0) *flag = *(volatile const int *)status;
+    __syncthreads();
+    return *flag != 0;
+}
+
+// Child domains: the parent's domain with the split coordinate as the left
+// child's upper and the right child's lower bound (the clip by the split
+// plane of the split-widest-dimension passage), plus their widest dimension.
+__device__ void write_child_domains(const float *dom_p, int k, int d, float split, float *dom_l, int *dim_l,
+                                    float *dom_r, int *dim_r) {
+    float lo[kMaxK], hi[kMaxK];
+    for (int c = 0; c < k; ++c) {
+        lo[c] = dom_p[c];
+        hi[c] = dom_p[k + c];
+    }
+    const float h = hi[d];
+    hi[d] = split;
+    for (int c = 0; c < k; ++c) {
+        dom_l[c] = lo[c];
+        dom_l[k + c] = hi[c];
+    }
+    *dim_l = widest_dim(lo, hi, k);
+    hi[d] = h;
+    lo[d] = split;
+    for (int c = 0; c < k; ++c) {
+        dom_r[c] = lo[c];
+        dom_r[k + c] = hi[c];
+    }
+    *dim_r = widest_dim(lo, hi, k);
+}
+
+// Exclusive block scan of a 64-bit value; `total` receives the block sum.
+__device__ __forceinline__ unsigned long long block_scan64(unsigned long long v, unsigned long long *red,
+                                                           unsigned long long &total) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= (uint32_t)o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) red[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        unsigned long long t = lane < (uint32_t)nw ? red[lane] : 0ull;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= (uint32_t)o) t += y;
+        }
+        red[lane] = t;
+    }
+    __syncthreads();
+    total = red[nw - 1];
+    return (w > 0 ? red[w - 1] : 0ull) + x - v;
+}
+
+// ---- partition of one tile ----------------------------------------------------
+
+// Side of a point relative to the split bucket: 0 left, 1 candidate, 2 right.
+// Certain-left points fill lChild's range from its start, certain-right ones
+// fill rChild's range from its end, candidates take slots 0..cnt-1 of the
+// candidate buffer (slot cnt-1 is position s, the node's own, unused, array
+// position; the others are the gap between the two certain groups).
+struct PartPlan {
+    uint32_t bstar, below, cnt, above;
+    int64_t right_tail;  // first position of the certain-right group
+};
+
+__device__ __forceinline__ int64_t cand_pos(const SegInfo &g, const PartPlan &pp, uint32_t slot) {
+    return slot + 1u < pp.cnt ? g.left_begin + pp.below + slot : g.s;
+}
+
+// `cursors` points at three counters (left, candidate, right) in shared or
+// global memory; `fh` is the fused children's histogram in shared memory, or
+// null.
+__device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
+                          int64_t pe, uint32_t *cursors, unsigned long long *red64, uint32_t *bases, uint32_t *fh,
+                          const Bucketer &bkc, int dn) {
+    const int64_t N = a.S.N;
+    const int k = a.k, d = g.d;
+    const uint32_t tid = threadIdx.x, nt = blockDim.x;
+    uint32_t key[kEPT];
+    int side[kEPT];
+    uint32_t cL = 0, cC = 0, cR = 0;
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) {
+        const int64_t q = t0 + (int64_t)i * nt + tid;
+        side[i] = 3;
+        if (q < pe) {
+            key[i] = a.src_keys[(int64_t)d * N + q];
+            const uint32_t b = (uint32_t)bk(key[i]);
+            side[i] = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
+            cL += side[i] == 0;
+            cC += side[i] == 1;
+            cR += side[i] == 2;
+        }
+    }
+    const unsigned long long packed = (unsigned long long)cL | ((unsigned long long)cC << 21) |
+                                      ((unsigned long long)cR << 42);
+    unsigned long long total;
+    const unsigned long long ex = block_scan64(packed, red64, total);
+    if (tid == 0) {
+        const uint32_t tL = (uint32_t)(total & 0x1fffffu), tC = (uint32_t)((total >> 21) & 0x1fffffu),
+                       tR = (uint32_t)(total >> 42);
+        bases[0] = tL ? atomicAdd(&cursors[0], tL) : 0u;
+        bases[1] = tC ? atomicAdd(&cursors[1], tC) : 0u;
+        bases[2] = tR ? atomicAdd(&cursors[2], tR) : 0u;
+    }
+    __syncthreads();
+    uint32_t oL = bases[0] + (uint32_t)(ex & 0x1fffffu);
+    uint32_t oC = bases[1] + (uint32_t)((ex >> 21) & 0x1fffffu);
+    uint32_t oR = bases[2] + (uint32_t)(ex >> 42);
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) {
+        if (side[i] == 3) continue;
+        const int64_t q = t0 + (int64_t)i * nt + tid;
+        int64_t pos;
+        bool ok;
+        uint32_t *ok_keys, *ok_idx;
+        if (side[i] == 0) {
+            ok = oL < pp.below;
+            pos = g.left_begin + oL++;
+            ok_keys = a.dst_keys;
+            ok_idx = a.dst_idx;
+        } else if (side[i] == 2) {
+            ok = oR < pp.above;
+            pos = pp.right_tail + oR++;
+            ok_keys = a.dst_keys;
+            ok_idx = a.dst_idx;
+        } else {
+            ok = oC < pp.cnt;
+            pos = cand_pos(g, pp, oC++);
+            ok_keys = a.cand_keys;
+            ok_idx = a.cand_idx;
+        }
+        if (!ok) {
+            set_status(a.status, KDT_EINTERNAL);
+            continue;
+        }
+        for (int c = 0; c < k; ++c) {
+            const uint32_t v = c == d ? key[i] : a.src_keys[(int64_t)c * N + q];
+            ok_keys[(int64_t)c * N + pos] = v;
+            if (fh != nullptr && c == dn && side[i] != 1) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(v)], 1u);
+        }
+        ok_idx[pos] = a.src_idx[q];
+    }
+}
+
+// ---- exact resolve of the candidates -----------------------------------------
+
+// Word i of candidate slot q (split order of dimension d).
+struct CandAcc {
+    const uint32_t *keys, *idx;
+    int64_t N, gap_begin, s;
+    uint32_t cnt;
+    int k, d;
+    __device__ __forceinline__ int64_t pos(uint32_t q) const { return q + 1u < cnt ? gap_begin + q : s; }
+    __device__ __forceinline__ uint32_t operator()(int i, uint32_t q) const {
+        const int64_t p = pos(q);
+        if (i == k) return idx[p];
+        int c = d + i;
+        if (c >= k) c -= k;
+        return keys[(int64_t)c * N + p];
+    }
+};
+
+// CTA-wide: selects the split point among the candidates, writes perm[s] and
+// the children's node-table entries, and moves the other candidates into the
+// gap between the certain groups.  `fuse`: add the candidates to the
+// children's histograms of the next level.
+__device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const PartPlan &pp, SelState &st,
+                                uint32_t *hist, uint32_t *red, uint32_t *medw, uint32_t *cur2, bool fuse, int dn) {
+    const uint32_t tid = threadIdx.x, nt = blockDim.x;
+    const int k = a.k;
+    const int64_t N = a.S.N;
+    const uint32_t r = g.m - pp.below;  // rank of the split point among the candidates
+    const CandAcc acc{a.cand_keys, a.cand_idx, N, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
+    cta_select(acc, pp.cnt, r, k + 1, st, hist, red);
+    if (st.err) {
+        if (tid == 0) set_status(a.status, KDT_EINTERNAL);
+        return;
+    }
+    if (tid <= (uint32_t)k) medw[tid] = acc((int)tid, st.med_q);
+    if (tid < 2) cur2[tid] = 0u;
+    __syncthreads();
+    Bucketer bkc;
+    bkc.lo = 0.f;
+    bkc.scale = 0.f;
+    if (fuse) bkc = seg_bucketer(a, g.j, dn);
+    const uint32_t lane = tid & 31u, lt = (1u << lane) - 1u;
+    const uint32_t nright = pp.cnt - 1u - r;
+    const int64_t right_begin = g.left_begin + g.m;
+    for (uint32_t q0 = 0; q0 < pp.cnt; q0 += nt) {
+        const uint32_t q = q0 + tid;
+        int side = -1;
+        if (q < pp.cnt) {
+            const int c = cmp_words(acc, q, medw, k + 1);
+            side = c < 0 ? 0 : (c > 0 ? 1 : -1);
+        }
+        const uint32_t lm = __ballot_sync(0xffffffffu, side == 0);
+        const uint32_t rm = __ballot_sync(0xffffffffu, side == 1);
+        uint32_t lb = 0, rb = 0;
+        if (lane == 0) {
+            if (lm) lb = atomicAdd(&cur2[0], __popc(lm));
+            if (rm) rb = atomicAdd(&cur2[1], __popc(rm));
+        }
+        lb = __shfl_sync(0xffffffffu, lb, 0);
+        rb = __shfl_sync(0xffffffffu, rb, 0);
+        if (side >= 0) {
+            int64_t pos;
+            bool ok;
+            if (side == 0) {
+                const uint32_t o = lb + __popc(lm & lt);
+                ok = o < r;
+                pos = g.left_begin + pp.below + o;
+            } else {
+                const uint32_t o = rb + __popc(rm & lt);
+                ok = o < nright;
+                pos = right_begin + o;
+            }
+            if (ok) {
+                const int64_t sp = acc.pos(q);
+                for (int c = 0; c < k; ++c) {
+                    const uint32_t v = a.cand_keys[(int64_t)c * N + sp];
+                    a.dst_keys[(int64_t)c * N + pos] = v;
+                    if (fuse && c == dn)
+                        atomicAdd(&a.hist_nxt[(2 * g.j + side) * kBuckets + bkc(v)], 1u);
+                }
+                a.dst_idx[pos] = a.cand_idx[sp];
+            } else {
+                set_status(a.status, KDT_EINTERNAL);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (cur2[0] != r || cur2[1] != nright) set_status(a.status, KDT_EINTERNAL);
+        a.perm[g.s] = (int32_t)medw[k];
+        write_child_domains(a.dom_cur + g.j * 2 * k, k, g.d, key2f(medw[0]), a.dom_nxt + (2 * g.j) * 2 * k,
+                            a.dim_nxt + 2 * g.j, a.dom_nxt + (2 * g.j + 1) * 2 * k, a.dim_nxt + 2 * g.j + 1);
+    }
+}
+
+// Picks the bucket holding rank m from a histogram of kBuckets counts
+// (CTA-wide).  Returns false if the counts do not add up to n.
+__device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out) {
+    const uint32_t tid = threadIdx.x, nt = blockDim.x;
+    const uint32_t per = kBuckets / nt;
+    uint32_t sum = 0;
+    for (uint32_t i = 0; i < per; ++i) sum += H[tid * per + i];
+    const uint32_t excl = block_exclusive_scan(sum, red);
+    const uint32_t total = red[(nt >> 5) - 1];
+    if (m >= excl && m < excl + sum) {
+        uint32_t c = excl;
+        for (uint32_t i = 0; i < per; ++i) {
+            const uint32_t h = H[tid * per + i];
+            if (m < c + h) {
+                out->bstar = tid * per + i;
+                out->below = c;
+                out->cnt = h;
+                out->above = n - c - h;
+                break;
+            }
+            c += h;
+        }
+    }
+    __syncthreads();
+    return total == n;
+}
+
+// ---- multi-CTA pipeline kernels ----------------------------------------------
+
+__global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
+    __shared__ uint32_t hist[kBuckets];
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    const int64_t begin = full_nodes(a.l) + (int64_t)blockIdx.x * a.per_cta;
+    const int64_t end = min(a.S.N, begin + a.per_cta);
+    const int64_t N = a.S.N;
+    for (int64_t p = begin; p < end;) {
+        const int64_t s = seg_of_pos(a.S, a.l, p);
+        const SegInfo g = seg_info(a, s);
+        const int64_t pe = min(end, g.base + (int64_t)g.n);
+        const Bucketer bk = seg_bucketer(a, g.j, g.d);
+        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
+        __syncthreads();
+        const uint32_t *col = a.src_keys + (int64_t)g.d * N;
+        for (int64_t q = p + threadIdx.x; q < pe; q += blockDim.x) atomicAdd(&hist[bk(col[q])], 1u);
+        __syncthreads();
+        uint32_t *H = a.hist_cur + g.j * kBuckets;
+        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x)
+            if (hist[b]) atomicAdd(&H[b], hist[b]);
+        __syncthreads();
+        p = pe;
+    }
+}
+
+__global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
+    __shared__ uint32_t red[64];
+    __shared__ PartPlan pp;
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    const int64_t s = full_nodes(a.l) + blockIdx.x;
+    const SegInfo g = seg_info(a, s);
+    const bool ok = pick_bucket(a.hist_cur + g.j * kBuckets, g.n, g.m, red, &pp);
+    if (threadIdx.x == 0) {
+        if (!ok) set_status(a.status, KDT_EINTERNAL);
+        SegSel sl;
+        sl.bstar = pp.bstar;
+        sl.below = pp.below;
+        sl.cnt = pp.cnt;
+        sl.curL = sl.curC = sl.curR = 0u;
+        a.sel[g.j] = sl;
+    }
+    if (a.hist_nxt) {
+        uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
+        for (uint32_t t = threadIdx.x; t < 2u * kBuckets; t += blockDim.x) H[t] = 0u;
+    }
+}
+
+__device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, uint32_t below, uint32_t cnt) {
+    PartPlan pp;
+    pp.bstar = bstar;
+    pp.below = below;
+    pp.cnt = cnt;
+    pp.above = g.n - below - cnt;
+    pp.right_tail = g.left_begin + g.m + (g.nr - pp.above);
+    return pp;
+}
+
+__global__ void __launch_bounds__(kLvlThreads, 2) level_part_kernel(LevelArgs a) {
+    __shared__ unsigned long long red64[32];
+    __shared__ uint32_t bases[3];
+    __shared__ uint32_t fh[2 * kBuckets];
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    const int64_t begin = full_nodes(a.l) + (int64_t)blockIdx.x * a.per_cta;
+    const int64_t end = min(a.S.N, begin + a.per_cta);
+    const bool fuse = a.hist_nxt != nullptr;
+    const int dn = (a.l + 1) % a.k;
+    for (int64_t p = begin; p < end;) {
+        const int64_t s = seg_of_pos(a.S, a.l, p);
+        const SegInfo g = seg_info(a, s);
+        const int64_t pe = min(end, g.base + (int64_t)g.n);
+        const Bucketer bk = seg_bucketer(a, g.j, g.d);
+        const SegSel sl = a.sel[g.j];
+        const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt);
+        Bucketer bkc;
+        bkc.lo = 0.f;
+        bkc.scale = 0.f;
+        if (fuse) {
+            bkc = seg_bucketer(a, g.j, dn);
+            for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
+        }
+        __syncthreads();
+        for (int64_t t0 = p; t0 < pe; t0 += kTile)
+            part_tile(a, g, bk, pp, t0, pe, &a.sel[g.j].curL, red64, bases, fuse ? fh : nullptr, bkc, dn);
+        __syncthreads();
+        if (fuse) {
+            uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
+            for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x)
+                if (fh[b]) atomicAdd(&H[b], fh[b]);
+            __syncthreads();
+        }
+        p = pe;
+    }
+}
+
+__global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a) {
+    __shared__ SelState st;
+    __shared__ uint32_t hist[kCtaRadixBins];
+    __shared__ uint32_t red[64];
+    __shared__ uint32_t medw[kMaxWords];
+    __shared__ uint32_t cur2[2];
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    const int64_t s = full_nodes(a.l) + blockIdx.x;
+    const SegInfo g = seg_info(a, s);
+    const SegSel sl = a.sel[g.j];
+    const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt);
+    if (sl.curL != pp.below || sl.curC != pp.cnt || sl.curR != pp.above) {
+        if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
+        return;
+    }
+    resolve_segment(a, g, pp, st, hist, red, medw, cur2, a.hist_nxt != nullptr, (a.l + 1) % a.k);
+}
+
+// ---- one CTA per subtree -------------------------------------------------------
+
+__global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) {
+    __shared__ SelState st;
+    __shared__ uint32_t hist[kBuckets];
+    __shared__ uint32_t red[64];
+    __shared__ unsigned long long red64[32];
+    __shared__ uint32_t bases[3];
+    __shared__ uint32_t cursors[3];
+    __shared__ uint32_t medw[kMaxWords];
+    __shared__ uint32_t cur2[2];
+    __shared__ PartPlan pps;
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    const int64_t s = full_nodes(a.l) + blockIdx.x;
+    const SegInfo g = seg_info(a, s);
+    const Bucketer bk = seg_bucketer(a, g.j, g.d);
+    const int64_t N = a.S.N;
+    const uint32_t *col = a.src_keys + (int64_t)g.d * N;
+    for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
+    if (threadIdx.x < 3) cursors[threadIdx.x] = 0u;
+    __syncthreads();
+    for (int64_t q = g.base + threadIdx.x; q < g.base + (int64_t)g.n; q += blockDim.x)
+        atomicAdd(&hist[bk(col[q])], 1u);
+    __syncthreads();
+    const bool ok = pick_bucket(hist, g.n, g.m, red, &pps);
+    if (!ok) {
+        if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
+        return;
+    }
+    const PartPlan pp = part_plan(g, pps.bstar, pps.below, pps.cnt);
+    Bucketer none;
+    none.lo = 0.f;
+    none.scale = 0.f;
+    for (int64_t t0 = g.base; t0 < g.base + (int64_t)g.n; t0 += kTile)
+        part_tile(a, g, bk, pp, t0, g.base + (int64_t)g.n, cursors, red64, bases, nullptr, none, 0);
+    __syncthreads();
+    if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
+        if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
+        return;
+    }
+    resolve_segment(a, g, pp, st, hist, red, medw, cur2, false, 0);
+}
+
+// ---- host side ------------------------------------------------------------------
+
+int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm, cudaStream_t stream) {
+    const Shape &S = p.S;
+    const int k = p.k;
+    LevelArgs a;
+    a.S = S;
+    a.k = k;
+    a.mode = p.mode;
+    a.l = l;
+    a.src_keys = b.keys[src];
+    a.src_idx = b.idx[src];
+    a.dst_keys = b.keys[src ^ 1];
+    a.dst_idx = b.idx[src ^ 1];
+    a.cand_keys = b.keys[2];
+    a.cand_idx = b.idx[2];
+    a.perm = perm;
+    a.dom_cur = b.dom[l & 1];
+    a.dim_cur = b.dim[l & 1];
+    a.dom_nxt = b.dom[(l + 1) & 1];
+    a.dim_nxt = b.dim[(l + 1) & 1];
+    a.hist_cur = b.hist[l & 1];
+    a.hist_nxt = nullptr;
+    a.sel = b.sel;
+    a.status = b.status;
+    a.per_cta = 0;
+    const int64_t nseg = nodes_on_level(S, l);
+    const int64_t live = S.N - full_nodes(l);
+    const double alg = 20.0 * (double)live;
+    const bool fusable = p.mode == KDT_SPLIT_ROUND_ROBIN && k >= 2;
+    if (l < p.multi_levels) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+        const int64_t grid = (int64_t)sms * 3;
+        a.per_cta = (live + grid - 1) / grid;
+        const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
+        const bool fused_here = l > 0 && fusable;
+        if (l + 1 < p.multi_levels && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
+        if (!fused_here) {
+            if (cudaMemsetAsync(a.hist_cur, 0, (size_t)nseg * kBuckets * 4, stream) != cudaSuccess) return KDT_ECUDA;
+            ProfScope ps(stream, "hist", 0.0);
+            level_hist_kernel<<<(unsigned)nblk, kLvlThreads, 0, stream>>>(a);
+            if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        }
+        {
+            ProfScope ps(stream, "pick", 0.0);
+            level_pick_kernel<<<(unsigned)nseg, kPickThreads, 0, stream>>>(a);
+            if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        }
+        {
+            ProfScope ps(stream, "part", alg);
+            level_part_kernel<<<(unsigned)nblk, kLvlThreads, 0, stream>>>(a);
+            if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        }
+        {
+            ProfScope ps(stream, "resolve", 0.0);
+            level_resolve_kernel<<<(unsigned)nseg, kLvlThreads, 0, stream>>>(a);
+            if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        }
+    } else {
+        ProfScope ps(stream, "seg", alg);
+        level_seg_kernel<<<(unsigned)nseg, kLvlThreads, 0, stream>>>(a);
+        if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+    }
+    return KDT_OK;
+}
+
+}  // namespace kdt
