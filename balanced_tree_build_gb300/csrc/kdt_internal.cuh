@@ -165,6 +165,10 @@ struct Buffers {
 
 Buffers carve(const Plan &p, void *base);
 
+// Finisher tile choice and launch (kdt_finisher.cu).
+int pick_tile(int k, int mode, int *T, size_t *smem);
+int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream);
+
 // Enqueues one global level l (records move from buffer src to src^1).
 int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm, cudaStream_t stream);
 

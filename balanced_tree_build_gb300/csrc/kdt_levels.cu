@@ -242,39 +242,49 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     uint32_t oL = bases[0] + (uint32_t)(ex & 0x1fffffu);
     uint32_t oC = bases[1] + (uint32_t)((ex >> 21) & 0x1fffffu);
     uint32_t oR = bases[2] + (uint32_t)(ex >> 42);
+    // destinations first, then one column at a time: all loads of a column
+    // are issued before any of its stores, so a thread waits for one memory
+    // latency per column rather than one per word
+    uint32_t pos[kEPT];
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
+        pos[i] = 0u;
         if (side[i] == 3) continue;
-        const int64_t q = t0 + (int64_t)i * nt + tid;
-        int64_t pos;
         bool ok;
-        uint32_t *ok_keys, *ok_idx;
         if (side[i] == 0) {
             ok = oL < pp.below;
-            pos = g.left_begin + oL++;
-            ok_keys = a.dst_keys;
-            ok_idx = a.dst_idx;
+            pos[i] = (uint32_t)(g.left_begin + oL++);
         } else if (side[i] == 2) {
             ok = oR < pp.above;
-            pos = pp.right_tail + oR++;
-            ok_keys = a.dst_keys;
-            ok_idx = a.dst_idx;
+            pos[i] = (uint32_t)(pp.right_tail + oR++);
         } else {
             ok = oC < pp.cnt;
-            pos = cand_pos(g, pp, oC++);
-            ok_keys = a.cand_keys;
-            ok_idx = a.cand_idx;
+            pos[i] = (uint32_t)cand_pos(g, pp, oC++);
         }
         if (!ok) {
             set_status(a.status, KDT_EINTERNAL);
-            continue;
+            side[i] = 3;
         }
-        for (int c = 0; c < k; ++c) {
-            const uint32_t v = c == d ? key[i] : a.src_keys[(int64_t)c * N + q];
-            ok_keys[(int64_t)c * N + pos] = v;
-            if (fh != nullptr && c == dn && side[i] != 1) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(v)], 1u);
+    }
+    for (int c = 0; c <= k; ++c) {
+        const uint32_t *scol = c < k ? a.src_keys + (int64_t)c * N : a.src_idx;
+        uint32_t *dcol = c < k ? a.dst_keys + (int64_t)c * N : a.dst_idx;
+        uint32_t *ccol = c < k ? a.cand_keys + (int64_t)c * N : a.cand_idx;
+        uint32_t v[kEPT];
+        if (c == d) {
+#pragma unroll
+            for (int i = 0; i < kEPT; ++i) v[i] = key[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < kEPT; ++i)
+                if (side[i] != 3) v[i] = __ldg(scol + t0 + (int64_t)i * nt + tid);
         }
-        ok_idx[pos] = a.src_idx[q];
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i) {
+            if (side[i] == 3) continue;
+            (side[i] == 1 ? ccol : dcol)[pos[i]] = v[i];
+            if (fh != nullptr && c == dn && side[i] != 1) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(v[i])], 1u);
+        }
     }
 }
 
@@ -380,8 +390,8 @@ __device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t 
     const uint32_t per = kBuckets / nt;
     uint32_t sum = 0;
     for (uint32_t i = 0; i < per; ++i) sum += H[tid * per + i];
-    const uint32_t excl = block_exclusive_scan(sum, red);
-    const uint32_t total = red[(nt >> 5) - 1];
+    uint32_t total;
+    const uint32_t excl = group_exclusive_scan(CtaGroup{}, sum, red, total);
     if (m >= excl && m < excl + sum) {
         uint32_t c = excl;
         for (uint32_t i = 0; i < per; ++i) {

@@ -1,5 +1,5 @@
-// kdt_select.cuh -- exact rank selection under the split order, for a CTA or
-// a warp.
+// kdt_select.cuh -- exact rank selection under the split order, for a CTA, a
+// group of warps, or one warp.
 //
 // The tree needs, for each subtree s, the point of 0-based rank ss(lChild(s))
 // among s's points under the strict order of its split dimension d: the
@@ -10,14 +10,16 @@
 // that the balance condition fixes).
 //
 // A point's order key is the word sequence w_0..w_k with w_i the
-// order-preserving key of x[(d+i) mod k] and w_k the input index.  The
-// selection is a most-significant-digit radix select over that sequence: each
-// round narrows the set of "matching" points (those that share the chosen
-// prefix) until one remains.  A round first takes min and max of the current
-// word over the matching points; if they agree the word is fixed, otherwise
-// the highest differing bit positions the next digit and a histogram of that
-// digit picks the bucket holding the wanted rank.  Because w_k is unique the
-// loop ends with exactly one point.
+// order-preserving key of x[(d+i) mod k] and w_k the input index.  The select
+// narrows the set of "matching" points round by round until one remains:
+//   * first round: value buckets evenly spread over [min, max] of x[d] among
+//     the points (a monotone function of w_0); for spread-out data this alone
+//     leaves one or a few points;
+//   * then most-significant-digit rounds over the words: min and max of the
+//     current word among the matching points; if equal the word is fixed,
+//     otherwise a histogram of the digit below the highest differing bit
+//     picks the bucket that holds the wanted rank.
+// Because w_k is unique the loop ends with exactly one point.
 #pragma once
 
 #include "kdt_internal.cuh"
@@ -37,13 +39,105 @@ struct SelState {
     uint32_t pv;
     uint32_t r;             // wanted rank among the matching points
     uint32_t cnt;           // number of matching points
-    uint32_t mn, mx;
+    int vb_on;              // value-bucket filter on w_0 active
+    uint32_t vb;
+    float vlo, vscale;
     uint32_t med_q;         // result: position of the selected point
     int err;
 };
 
+// ---- thread groups ------------------------------------------------------------
+
+// All threads of the CTA.
+struct CtaGroup {
+    __device__ __forceinline__ uint32_t tid() const { return threadIdx.x; }
+    __device__ __forceinline__ uint32_t size() const { return blockDim.x; }
+    __device__ __forceinline__ void sync() const { __syncthreads(); }
+};
+
+// `n` consecutive threads (whole warps) starting at thread `base`,
+// synchronised by named barrier `bar` (1..15); a single warp uses __syncwarp.
+struct WarpsGroup {
+    uint32_t base, n;
+    int bar;
+    __device__ __forceinline__ uint32_t tid() const { return threadIdx.x - base; }
+    __device__ __forceinline__ uint32_t size() const { return n; }
+    __device__ __forceinline__ void sync() const {
+        if (n == 32u) __syncwarp();
+        else asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(n) : "memory");
+    }
+};
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// min and max over the group (result in every thread); `red` >= 64 words.
+template <class G>
+__device__ __forceinline__ void group_minmax(const G &g, uint32_t &mn, uint32_t &mx, uint32_t *red) {
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const uint32_t nw = g.size() >> 5;
+    if (nw == 1u) return;
+    const uint32_t w = g.tid() >> 5;
+    g.sync();
+    if (lane_id() == 0) {
+        red[w] = mn;
+        red[32 + w] = mx;
+    }
+    g.sync();
+    uint32_t a = lane_id() < nw ? red[lane_id()] : 0xffffffffu;
+    uint32_t b = lane_id() < nw ? red[32 + lane_id()] : 0u;
+    mn = __reduce_min_sync(0xffffffffu, a);
+    mx = __reduce_max_sync(0xffffffffu, b);
+}
+
+// Exclusive scan of one value per thread over the group; `total` gets the sum.
+template <class G>
+__device__ __forceinline__ uint32_t group_exclusive_scan(const G &g, uint32_t v, uint32_t *red, uint32_t &total) {
+    const uint32_t lane = lane_id();
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= (uint32_t)o) x += y;
+    }
+    const uint32_t nw = g.size() >> 5;
+    if (nw == 1u) {
+        total = __shfl_sync(0xffffffffu, x, 31);
+        return x - v;
+    }
+    const uint32_t w = g.tid() >> 5;
+    g.sync();
+    if (lane == 31) red[w] = x;
+    g.sync();
+    uint32_t t = lane < nw ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= (uint32_t)o) t += y;
+    }
+    total = __shfl_sync(0xffffffffu, t, 31);
+    const uint32_t before = w > 0 ? __shfl_sync(0xffffffffu, t, (w - 1) & 31) : 0u;
+    return before + x - v;
+}
+
+// Block-wide exclusive scan (whole CTA).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *red) {
+    uint32_t total;
+    return group_exclusive_scan(CtaGroup{}, v, red, total);
+}
+
+// ---- matching ---------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t value_bucket(uint32_t key, float lo, float scale, uint32_t nb) {
+    const float t = __fmul_rn(__fsub_rn(key2f(key), lo), scale);
+    int b = __float2int_rz(t);
+    b = b < 0 ? 0 : b;
+    return (uint32_t)b < nb ? (uint32_t)b : nb - 1u;
+}
+
 template <class Acc>
-__device__ __forceinline__ bool sel_matches(const Acc &acc, const SelState &st, uint32_t q) {
+__device__ __forceinline__ bool sel_matches(const Acc &acc, const SelState &st, uint32_t q, uint32_t nb) {
+    if (st.vb_on && value_bucket(acc(0, q), st.vlo, st.vscale, nb) != st.vb) return false;
     for (int i = 0; i < st.j; ++i)
         if (acc(i, q) != st.f[i]) return false;
     if (st.has_prefix && (acc(st.j, q) >> st.sh) != st.pv) return false;
@@ -60,69 +154,16 @@ __device__ __forceinline__ int cmp_words(const Acc &acc, uint32_t q, const uint3
     return 0;
 }
 
-// ---- block-wide helpers (blockDim.x a multiple of 32, at most 1024) -------
-
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
-__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, uint32_t *red) {
-    mn = __reduce_min_sync(0xffffffffu, mn);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if (lane_id() == 0) {
-        red[w] = mn;
-        red[32 + w] = mx;
-    }
-    __syncthreads();
-    if (w == 0) {
-        uint32_t a = lane_id() < (uint32_t)nw ? red[lane_id()] : 0xffffffffu;
-        uint32_t b = lane_id() < (uint32_t)nw ? red[32 + lane_id()] : 0u;
-        a = __reduce_min_sync(0xffffffffu, a);
-        b = __reduce_max_sync(0xffffffffu, b);
-        if (lane_id() == 0) {
-            red[0] = a;
-            red[32] = b;
-        }
-    }
-    __syncthreads();
-    mn = red[0];
-    mx = red[32];
-}
-
-// Exclusive scan of one value per thread; returns the exclusive prefix.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *red) {
-    const uint32_t lane = lane_id();
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= (uint32_t)o) x += y;
-    }
-    __syncthreads();
-    if (lane == 31) red[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        uint32_t t = lane < (uint32_t)nw ? red[lane] : 0u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= (uint32_t)o) t += y;
-        }
-        red[lane] = t;  // inclusive warp totals
-    }
-    __syncthreads();
-    const uint32_t before = w > 0 ? red[w - 1] : 0u;
-    return before + x - v;
-}
-
-// CTA-wide exact select of rank m among n points (positions 0..n-1 through
-// `acc`).  On return (after a barrier) st.med_q holds the selected position.
-// `hist` holds kCtaRadixBins words; `red` at least 64 words.
-template <class Acc>
-__device__ void cta_select(const Acc &acc, uint32_t n, uint32_t m, int nwords, SelState &st,
-                           uint32_t *hist, uint32_t *red) {
-    const uint32_t tid = threadIdx.x, nt = blockDim.x;
+// Group-wide exact select of rank m among n points (positions 0..n-1 through
+// `acc`).  `hist` holds 2^bits words (2^bits a multiple of the group size),
+// `red` >= 64 words, `st` is the group's state; all in shared memory.  On
+// return (after a group barrier) st.med_q holds the selected position and
+// st.err is nonzero on an internal inconsistency.
+template <class G, class Acc>
+__device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m, int nwords, SelState &st,
+                             uint32_t *hist, int bits, uint32_t *red) {
+    const uint32_t tid = g.tid(), nt = g.size();
+    const uint32_t nbins = 1u << bits;
     if (tid == 0) {
         st.j = 0;
         st.has_prefix = 0;
@@ -130,172 +171,116 @@ __device__ void cta_select(const Acc &acc, uint32_t n, uint32_t m, int nwords, S
         st.pv = 0;
         st.r = m;
         st.cnt = n;
+        st.vb_on = 0;
+        st.vb = 0;
+        st.vlo = 0.f;
+        st.vscale = 0.f;
         st.err = 0;
         st.med_q = 0;
     }
-    __syncthreads();
-    for (int guard = 0; guard < 8 * kMaxWords; ++guard) {
+    g.sync();
+    bool value_round = true;
+    for (int guard = 0; guard < 8 * kMaxWords + 2; ++guard) {
         if (st.cnt <= 1u || st.j >= nwords) break;
         const int j = st.j;
         uint32_t mn = 0xffffffffu, mx = 0u;
         for (uint32_t q = tid; q < n; q += nt) {
-            if (sel_matches(acc, st, q)) {
+            if (sel_matches(acc, st, q, nbins)) {
                 const uint32_t w = acc(j, q);
                 mn = min(mn, w);
                 mx = max(mx, w);
             }
         }
-        block_minmax(mn, mx, red);
+        group_minmax(g, mn, mx, red);
         if (mn == mx) {
+            g.sync();
             if (tid == 0) {
                 st.f[j] = mn;
                 st.j = j + 1;
                 st.has_prefix = 0;
             }
-            __syncthreads();
+            g.sync();
+            value_round = false;
             continue;
         }
-        const int hb = 31 - __clz(mn ^ mx);
-        const int sh = hb - (kCtaRadixBits - 1) > 0 ? hb - (kCtaRadixBits - 1) : 0;
-        const uint32_t lo = mn >> sh;
-        for (uint32_t b = tid; b < (uint32_t)kCtaRadixBins; b += nt) hist[b] = 0u;
-        __syncthreads();
-        for (uint32_t q = tid; q < n; q += nt) {
-            if (sel_matches(acc, st, q)) atomicAdd(&hist[(acc(j, q) >> sh) - lo], 1u);
+        // this round's bucket function
+        bool vround = false;
+        float vlo = 0.f, vscale = 0.f;
+        int sh = 0;
+        uint32_t lo = 0;
+        if (value_round && j == 0) {
+            vlo = key2f(mn);
+            const float r = __fsub_rn(key2f(mx), vlo);
+            if (r > 0.f && r <= 3.0e38f) {
+                vscale = __fdiv_rn((float)nbins, r);
+                if (vscale <= 3.0e38f) vround = true;
+            }
         }
-        __syncthreads();
-        // find the bucket that holds rank r
-        const uint32_t per = kCtaRadixBins / nt;  // bins per thread (nt divides 2048)
+        value_round = false;
+        if (!vround) {
+            const int hb = 31 - __clz(mn ^ mx);
+            sh = hb - (bits - 1) > 0 ? hb - (bits - 1) : 0;
+            lo = mn >> sh;
+        }
+        for (uint32_t b = tid; b < nbins; b += nt) hist[b] = 0u;
+        g.sync();
+        for (uint32_t q = tid; q < n; q += nt) {
+            if (sel_matches(acc, st, q, nbins)) {
+                const uint32_t w = acc(j, q);
+                const uint32_t b = vround ? value_bucket(w, vlo, vscale, nbins) : (w >> sh) - lo;
+                atomicAdd(&hist[b], 1u);
+            }
+        }
+        g.sync();
+        const uint32_t per = nbins / nt;
         uint32_t sum = 0;
         for (uint32_t i = 0; i < per; ++i) sum += hist[tid * per + i];
-        const uint32_t excl = block_exclusive_scan(sum, red);
+        uint32_t total;
+        const uint32_t excl = group_exclusive_scan(g, sum, red, total);
         const uint32_t r = st.r;
-        __syncthreads();
+        g.sync();
         if (r >= excl && r < excl + sum) {
             uint32_t c = excl;
             for (uint32_t i = 0; i < per; ++i) {
                 const uint32_t h = hist[tid * per + i];
                 if (r < c + h) {
+                    const uint32_t b = tid * per + i;
                     st.r = r - c;
                     st.cnt = h;
-                    st.pv = lo + tid * per + i;
-                    st.sh = sh;
-                    st.has_prefix = 1;
-                    if (sh == 0) {
-                        st.f[j] = st.pv;
-                        st.j = j + 1;
-                        st.has_prefix = 0;
+                    if (vround) {
+                        st.vb_on = 1;
+                        st.vb = b;
+                        st.vlo = vlo;
+                        st.vscale = vscale;
+                    } else {
+                        st.pv = lo + b;
+                        st.sh = sh;
+                        st.has_prefix = 1;
+                        if (sh == 0) {
+                            st.f[j] = st.pv;
+                            st.j = j + 1;
+                            st.has_prefix = 0;
+                        }
                     }
                     break;
                 }
                 c += h;
             }
         }
-        __syncthreads();
+        g.sync();
     }
     if (st.cnt != 1u && tid == 0) st.err = 1;
-    __syncthreads();
+    g.sync();
     for (uint32_t q = tid; q < n; q += nt)
-        if (sel_matches(acc, st, q)) st.med_q = q;
-    __syncthreads();
+        if (sel_matches(acc, st, q, nbins)) st.med_q = q;
+    g.sync();
 }
 
-// Warp-wide exact select of rank m among n points.  All 32 lanes call it;
-// `wf` is per-warp scratch of kMaxWords words, `hist` kWarpRadixBins words.
-// Returns the selected position (same value in every lane), or 0xffffffff
-// on an internal inconsistency.
+// CTA-wide select with 2^11 buckets (global levels).
 template <class Acc>
-__device__ uint32_t warp_select(const Acc &acc, uint32_t n, uint32_t m, int nwords, uint32_t *wf,
-                                uint32_t *hist) {
-    const uint32_t lane = lane_id();
-    int j = 0, has_prefix = 0, sh = 0;
-    uint32_t pv = 0, r = m, cnt = n;
-    auto matches = [&](uint32_t q) -> bool {
-        for (int i = 0; i < j; ++i)
-            if (acc(i, q) != wf[i]) return false;
-        if (has_prefix && (acc(j, q) >> sh) != pv) return false;
-        return true;
-    };
-    for (int guard = 0; guard < 8 * kMaxWords && cnt > 1u && j < nwords; ++guard) {
-        uint32_t mn = 0xffffffffu, mx = 0u;
-        for (uint32_t q = lane; q < n; q += 32) {
-            if (matches(q)) {
-                const uint32_t w = acc(j, q);
-                mn = min(mn, w);
-                mx = max(mx, w);
-            }
-        }
-        mn = __reduce_min_sync(0xffffffffu, mn);
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (mn == mx) {
-            __syncwarp();
-            if (lane == 0) wf[j] = mn;
-            __syncwarp();
-            ++j;
-            has_prefix = 0;
-            continue;
-        }
-        const int hb = 31 - __clz(mn ^ mx);
-        const int nsh = hb - (kWarpRadixBits - 1) > 0 ? hb - (kWarpRadixBits - 1) : 0;
-        const uint32_t lo = mn >> nsh;
-#pragma unroll
-        for (int b = 0; b < kWarpRadixBins / 32; ++b) hist[lane + 32 * b] = 0u;
-        __syncwarp();
-        for (uint32_t q = lane; q < n; q += 32)
-            if (matches(q)) atomicAdd(&hist[(acc(j, q) >> nsh) - lo], 1u);
-        __syncwarp();
-        constexpr int per = kWarpRadixBins / 32;
-        uint32_t h[per];
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < per; ++i) {
-            h[i] = hist[lane * per + i];
-            sum += h[i];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= (uint32_t)o) incl += y;
-        }
-        const uint32_t excl = incl - sum;
-        const bool mine = r >= excl && r < incl;
-        uint32_t nr = 0, ncnt = 0, npv = 0;
-        if (mine) {
-            uint32_t c = excl;
-#pragma unroll
-            for (int i = 0; i < per; ++i) {
-                if (r >= c && r < c + h[i]) {
-                    nr = r - c;
-                    ncnt = h[i];
-                    npv = lo + lane * per + i;
-                }
-                c += h[i];
-            }
-        }
-        const uint32_t who = __ballot_sync(0xffffffffu, mine);
-        if (who == 0u) return 0xffffffffu;
-        const int src = __ffs(who) - 1;
-        r = __shfl_sync(0xffffffffu, nr, src);
-        cnt = __shfl_sync(0xffffffffu, ncnt, src);
-        pv = __shfl_sync(0xffffffffu, npv, src);
-        sh = nsh;
-        has_prefix = 1;
-        if (sh == 0) {
-            __syncwarp();
-            if (lane == 0) wf[j] = pv;
-            __syncwarp();
-            ++j;
-            has_prefix = 0;
-        }
-        __syncwarp();
-    }
-    if (cnt != 1u) return 0xffffffffu;
-    uint32_t found = 0xffffffffu;
-    for (uint32_t q = lane; q < n; q += 32)
-        if (matches(q)) found = q;
-    found = __reduce_min_sync(0xffffffffu, found);
-    return found;
+__device__ __forceinline__ void cta_select(const Acc &acc, uint32_t n, uint32_t m, int nwords, SelState &st,
+                                           uint32_t *hist, uint32_t *red) {
+    group_select(CtaGroup{}, acc, n, m, nwords, st, hist, kCtaRadixBits, red);
 }
 
 }  // namespace kdt
