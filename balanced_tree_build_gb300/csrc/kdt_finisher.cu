@@ -10,11 +10,12 @@
 // Inside the CTA the records stay put; a list of 16-bit local ids is
 // partitioned level by level (ping-pong).  The work is split by node size:
 //   * phase A (nodes > 256 points): the nodes of a level are spread over
-//     warp groups (16 / nodes warps each, named barriers), each group runs an
-//     exact select and a partition;
-//   * phase B (nodes <= 256): each warp owns whole subtrees; nodes > 32 use a
-//     warp select, nodes <= 32 rank their points with one lane per point,
-//     subtrees of <= 7 points are finished by one lane each.
+//     warp groups (16 / nodes warps each, named barriers); each group splits
+//     its node by value buckets (min/max, one histogram, one partition pass)
+//     and ranks the few points of the split bucket exactly;
+//   * phase B (nodes <= 256): each warp owns whole subtrees; nodes > 32 are
+//     split the same way by one warp, nodes <= 32 rank their points with one
+//     lane per point, subtrees of <= 7 points are finished by one lane each.
 // Phase-B subtrees are laid out relative to the range the warp took over, so
 // warps never touch each other's ranges.
 #include "kdt_internal.cuh"
@@ -26,6 +27,7 @@ constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kWarpMax = 256;  // phase B: subtrees this small go to one warp
 constexpr int kLaneMax = 7;    // subtrees this small go to one lane
+constexpr int kCandPerWarp = 64;  // bucket-split candidates per warp
 constexpr size_t kFinSmemBudget = 200 * 1024;
 constexpr int kFinHistWords = kFinWarps * kWarpRadixBins;  // 4096
 
@@ -219,6 +221,133 @@ __device__ void group_split_node(const G &grp, const FinArgs &a, const FinSmem &
     grp.sync();
 }
 
+// Group-wide split of node u by value buckets: min and max of the split
+// coordinate, one histogram of 2^bits buckets over that range, one partition
+// pass (points below the split bucket go left, above it right); the few
+// points in the split bucket ("candidates", at most `cap`, listed in `cand`)
+// are then ranked exactly by pairwise comparison under the full split order.
+// Falls back to the exact select when the split coordinate is constant or
+// the candidates do not fit.  `pk` holds 8 words of shared scratch.
+template <class G>
+__device__ void group_bucket_split(const G &grp, const FinArgs &a, const FinSmem &sm, int64_t s0, int j, int64_t u,
+                                   const NodeGeom &ng, const uint16_t *src_all, uint16_t *dst, SelState &st,
+                                   uint32_t *hist, int bits, uint32_t *red, uint32_t *medw, uint32_t *pk,
+                                   uint16_t *cand, uint32_t cap) {
+    const int k = a.k, T = a.T;
+    const int d = fin_dim(a, sm, s0, j, u);
+    const uint16_t *src = src_all + ng.off;
+    const uint32_t tid = grp.tid(), nt = grp.size();
+    const uint32_t nb = 1u << bits;
+    const uint32_t *kd = sm.keys + d * T;
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (uint32_t q = tid; q < ng.n; q += nt) {
+        const uint32_t v = kd[src[q]];
+        mn = min(mn, v);
+        mx = max(mx, v);
+    }
+    group_minmax(grp, mn, mx, red);
+    const float lo = key2f(mn);
+    const float rg = __fsub_rn(key2f(mx), lo);
+    float scale = 0.f;
+    if (rg > 0.f && rg <= 3.0e38f) scale = __fdiv_rn((float)nb, rg);
+    if (mn == mx || !(scale > 0.f && scale <= 3.0e38f)) {
+        grp.sync();
+        group_split_node(grp, a, sm, s0, j, u, ng, src_all, dst, st, hist, bits, red, medw, pk);
+        return;
+    }
+    for (uint32_t b = tid; b < nb; b += nt) hist[b] = 0u;
+    grp.sync();
+    for (uint32_t q = tid; q < ng.n; q += nt) atomicAdd(&hist[value_bucket(kd[src[q]], lo, scale, nb)], 1u);
+    grp.sync();
+    {
+        const uint32_t per = nb / nt;
+        uint32_t sum = 0;
+        for (uint32_t i = 0; i < per; ++i) sum += hist[tid * per + i];
+        uint32_t total;
+        const uint32_t excl = group_exclusive_scan(grp, sum, red, total);
+        if (ng.m >= excl && ng.m < excl + sum) {
+            uint32_t c = excl;
+            for (uint32_t i = 0; i < per; ++i) {
+                const uint32_t h = hist[tid * per + i];
+                if (ng.m < c + h) {
+                    pk[0] = tid * per + i;
+                    pk[1] = c;
+                    pk[2] = h;
+                    break;
+                }
+                c += h;
+            }
+        }
+        if (tid < 3) pk[4 + tid] = 0u;
+    }
+    grp.sync();
+    const uint32_t bstar = pk[0], below = pk[1], cnt = pk[2];
+    if (cnt > cap) {
+        grp.sync();
+        group_split_node(grp, a, sm, s0, j, u, ng, src_all, dst, st, hist, bits, red, medw, pk);
+        return;
+    }
+    const uint32_t above = ng.n - below - cnt;
+    const uint32_t nr = ng.n - ng.m - 1u;
+    const uint32_t right_tail = ng.right_off + (nr - above);
+    const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
+    for (uint32_t q0 = 0; q0 < ng.n; q0 += nt) {
+        const uint32_t q = q0 + tid;
+        int side = 3;
+        uint32_t id = 0;
+        if (q < ng.n) {
+            id = src[q];
+            const uint32_t b = value_bucket(kd[id], lo, scale, nb);
+            side = b < bstar ? 0 : (b > bstar ? 2 : 1);
+        }
+        const uint32_t lm = __ballot_sync(0xffffffffu, side == 0);
+        const uint32_t cm = __ballot_sync(0xffffffffu, side == 1);
+        const uint32_t rm = __ballot_sync(0xffffffffu, side == 2);
+        uint32_t lb = 0, cb = 0, rb = 0;
+        if (lane == 0) {
+            if (lm) lb = atomicAdd(&pk[4], __popc(lm));
+            if (cm) cb = atomicAdd(&pk[5], __popc(cm));
+            if (rm) rb = atomicAdd(&pk[6], __popc(rm));
+        }
+        lb = __shfl_sync(0xffffffffu, lb, 0);
+        cb = __shfl_sync(0xffffffffu, cb, 0);
+        rb = __shfl_sync(0xffffffffu, rb, 0);
+        if (side == 0) {
+            const uint32_t o = lb + __popc(lm & lt);
+            if (o < below) dst[ng.left_off + o] = (uint16_t)id;
+            else set_status(a.status, KDT_EINTERNAL);
+        } else if (side == 2) {
+            const uint32_t o = rb + __popc(rm & lt);
+            if (o < above) dst[right_tail + o] = (uint16_t)id;
+            else set_status(a.status, KDT_EINTERNAL);
+        } else if (side == 1) {
+            const uint32_t o = cb + __popc(cm & lt);
+            if (o < cnt) cand[o] = (uint16_t)id;
+            else set_status(a.status, KDT_EINTERNAL);
+        }
+    }
+    grp.sync();
+    // exact ranks of the candidates; rank r = m - below is the split point
+    const uint32_t r = ng.m - below;
+    for (uint32_t q = tid; q < cnt; q += nt) {
+        const uint32_t id = cand[q];
+        uint32_t rank = 0;
+        for (uint32_t t = 0; t < cnt; ++t) {
+            const uint32_t o = cand[t];
+            if (o != id && local_less(sm, T, k, d, o, id)) ++rank;
+        }
+        if (rank == r) {
+            a.perm[u] = (int32_t)sm.idx[id];
+            record_split(a, sm, s0, j, u, id, d);
+        } else if (rank < r) {
+            dst[ng.left_off + below + rank] = (uint16_t)id;
+        } else {
+            dst[ng.right_off + rank - r - 1u] = (uint16_t)id;
+        }
+    }
+    grp.sync();
+}
+
 // Warp: split node u of at most 32 points, one lane per point.  The rank of
 // each point comes from a 32-bucket value ranking (five ballots); if two
 // points share a bucket, from all-pairs comparisons.
@@ -343,7 +472,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
     __shared__ SelState st[kFinWarps];
     __shared__ uint32_t red[kFinWarps][64];
     __shared__ uint32_t medw[kFinWarps][kMaxWords];
-    __shared__ uint32_t cur2[kFinWarps][2];
+    __shared__ uint32_t pk[kFinWarps][8];
+    __shared__ uint16_t cand[kFinWarps * kCandPerWarp];
     __shared__ int stop;
     const uint32_t tid = threadIdx.x;
     if (tid == 0) stop = *(volatile int *)a.status;
@@ -389,8 +519,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
         for (int64_t o = g; o < count; o += ng) {
             const int64_t u = first + o;
             const NodeGeom geom = node_geom(S, s0, a.l0, 0u, j, u);
-            group_split_node(grp, a, sm, s0, j, u, geom, sm.ids[cur], sm.ids[cur ^ 1], st[g], hist, bits, red[g],
-                             medw[g], cur2[g]);
+            group_bucket_split(grp, a, sm, s0, j, u, geom, sm.ids[cur], sm.ids[cur ^ 1], st[g], hist, bits, red[g],
+                               medw[g], pk[g], cand + g * wpg * kCandPerWarp, wpg * kCandPerWarp);
         }
         __syncthreads();
         cur ^= 1;
@@ -428,8 +558,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
                     const int64_t u = f + oo;
                     const NodeGeom geom = node_geom(S, t, j, off_t, jj, u);
                     if (geom.n > 32u)
-                        group_split_node(wg, a, sm, s0, jj, u, geom, sm.ids[c], sm.ids[c ^ 1], st[w], hist,
-                                         kWarpRadixBits, red[w], medw[w], cur2[w]);
+                        group_bucket_split(wg, a, sm, s0, jj, u, geom, sm.ids[c], sm.ids[c ^ 1], st[w], hist,
+                                           kWarpRadixBits, red[w], medw[w], pk[w], cand + w * kCandPerWarp,
+                                           (uint32_t)kCandPerWarp);
                     else
                         warp_split_small(a, sm, s0, jj, u, geom, sm.ids[c], sm.ids[c ^ 1]);
                 }

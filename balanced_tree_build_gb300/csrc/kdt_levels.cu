@@ -33,7 +33,8 @@ namespace kdt {
 
 constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
-constexpr int kEPT = 8;                          // points per thread per tile
+constexpr int kEPT = 4;                          // points per thread per tile
+constexpr int kPre = 4;                          // key columns loaded ahead in a tile
 constexpr int kTile = kLvlThreads * kEPT;
 
 // ---- value buckets ----------------------------------------------------------
@@ -203,82 +204,144 @@ __device__ __forceinline__ int64_t cand_pos(const SegInfo &g, const PartPlan &pp
 }
 
 // `cursors` points at three counters (left, candidate, right) in shared or
-// global memory; `fh` is the fused children's histogram in shared memory, or
-// null.
+// global memory; `wtot` and `wbase` are 3 words per warp of shared scratch;
+// `fh` is the fused children's histogram in shared memory, or null.
+//
+// Output order is slot-major per warp: for each of a thread's kEPT points the
+// warp's lanes going to one side write consecutive positions (ballot +
+// popcount), so every warp store covers one contiguous run.
 __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
-                          int64_t pe, uint32_t *cursors, unsigned long long *red64, uint32_t *bases, uint32_t *fh,
+                          int64_t pe, uint32_t *cursors, uint32_t *wtot, uint32_t *wbase, uint32_t *fh,
                           const Bucketer &bkc, int dn) {
     const int64_t N = a.S.N;
     const int k = a.k, d = g.d;
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
-    uint32_t key[kEPT];
-    int side[kEPT];
-    uint32_t cL = 0, cC = 0, cR = 0;
+    const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    // Every word of the tile's records that fits the register budget is
+    // loaded here, before the reservation, so a thread waits for about one
+    // memory latency per tile: [c][i] holds key column c (c < kPre) and, at
+    // c = kPre, the input index.
+    uint32_t pv[kPre + 1][kEPT];
+    uint32_t mL[kEPT], mR[kEPT], mC[kEPT];
+    uint32_t tL = 0, tC = 0, tR = 0;
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         const int64_t q = t0 + (int64_t)i * nt + tid;
-        side[i] = 3;
-        if (q < pe) {
-            key[i] = a.src_keys[(int64_t)d * N + q];
-            const uint32_t b = (uint32_t)bk(key[i]);
-            side[i] = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
-            cL += side[i] == 0;
-            cC += side[i] == 1;
-            cR += side[i] == 2;
+        const bool valid = q < pe;
+#pragma unroll
+        for (int c = 0; c <= kPre; ++c) {
+            pv[c][i] = 0u;
+            if (valid && (c == kPre || c < k)) pv[c][i] = __ldg((c == kPre ? a.src_idx : a.src_keys + (int64_t)c * N) + q);
         }
     }
-    const unsigned long long packed = (unsigned long long)cL | ((unsigned long long)cC << 21) |
-                                      ((unsigned long long)cR << 42);
-    unsigned long long total;
-    const unsigned long long ex = block_scan64(packed, red64, total);
-    if (tid == 0) {
-        const uint32_t tL = (uint32_t)(total & 0x1fffffu), tC = (uint32_t)((total >> 21) & 0x1fffffu),
-                       tR = (uint32_t)(total >> 42);
-        bases[0] = tL ? atomicAdd(&cursors[0], tL) : 0u;
-        bases[1] = tC ? atomicAdd(&cursors[1], tC) : 0u;
-        bases[2] = tR ? atomicAdd(&cursors[2], tR) : 0u;
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) {
+        const int64_t q = t0 + (int64_t)i * nt + tid;
+        int side = 3;
+        if (q < pe) {
+            uint32_t key = pv[0][i];  // static indices keep pv in registers
+#pragma unroll
+            for (int c = 1; c < kPre; ++c)
+                if (d == c) key = pv[c][i];
+            if (d >= kPre) key = __ldg(a.src_keys + (int64_t)d * N + q);
+            const uint32_t b = (uint32_t)bk(key);
+            side = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
+        }
+        mL[i] = __ballot_sync(0xffffffffu, side == 0);
+        mC[i] = __ballot_sync(0xffffffffu, side == 1);
+        mR[i] = __ballot_sync(0xffffffffu, side == 2);
+        tL += __popc(mL[i]);
+        tC += __popc(mC[i]);
+        tR += __popc(mR[i]);
+    }
+    if (lane == 0) {
+        wtot[3 * w + 0] = tL;
+        wtot[3 * w + 1] = tC;
+        wtot[3 * w + 2] = tR;
     }
     __syncthreads();
-    uint32_t oL = bases[0] + (uint32_t)(ex & 0x1fffffu);
-    uint32_t oC = bases[1] + (uint32_t)((ex >> 21) & 0x1fffffu);
-    uint32_t oR = bases[2] + (uint32_t)(ex >> 42);
-    // destinations first, then one column at a time: all loads of a column
-    // are issued before any of its stores, so a thread waits for one memory
-    // latency per column rather than one per word
+    if (w == 0) {
+        // exclusive prefix over warps, then one reservation per side
+        uint32_t v[3], x[3];
+#pragma unroll
+        for (int sd = 0; sd < 3; ++sd) {
+            v[sd] = lane < nw ? wtot[3 * lane + sd] : 0u;
+            x[sd] = v[sd];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x[sd], o);
+                if (lane >= (uint32_t)o) x[sd] += y;
+            }
+        }
+        uint32_t base[3] = {0u, 0u, 0u};
+        if (lane == 31) {
+#pragma unroll
+            for (int sd = 0; sd < 3; ++sd) base[sd] = x[sd] ? atomicAdd(&cursors[sd], x[sd]) : 0u;
+        }
+#pragma unroll
+        for (int sd = 0; sd < 3; ++sd) {
+            base[sd] = __shfl_sync(0xffffffffu, base[sd], 31);
+            if (lane < nw) wbase[3 * lane + sd] = base[sd] + x[sd] - v[sd];
+        }
+    }
+    __syncthreads();
+    uint32_t oL = wbase[3 * w + 0], oC = wbase[3 * w + 1], oR = wbase[3 * w + 2];
     uint32_t pos[kEPT];
+    int side[kEPT];
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         pos[i] = 0u;
-        if (side[i] == 3) continue;
-        bool ok;
-        if (side[i] == 0) {
-            ok = oL < pp.below;
-            pos[i] = (uint32_t)(g.left_begin + oL++);
-        } else if (side[i] == 2) {
-            ok = oR < pp.above;
-            pos[i] = (uint32_t)(pp.right_tail + oR++);
-        } else {
-            ok = oC < pp.cnt;
-            pos[i] = (uint32_t)cand_pos(g, pp, oC++);
+        side[i] = 3;
+        const uint32_t bit = 1u << lane;
+        bool ok = true;
+        if (mL[i] & bit) {
+            const uint32_t o = oL + __popc(mL[i] & lt);
+            ok = o < pp.below;
+            pos[i] = (uint32_t)(g.left_begin + o);
+            side[i] = 0;
+        } else if (mR[i] & bit) {
+            const uint32_t o = oR + __popc(mR[i] & lt);
+            ok = o < pp.above;
+            pos[i] = (uint32_t)(pp.right_tail + o);
+            side[i] = 2;
+        } else if (mC[i] & bit) {
+            const uint32_t o = oC + __popc(mC[i] & lt);
+            ok = o < pp.cnt;
+            pos[i] = (uint32_t)cand_pos(g, pp, o);
+            side[i] = 1;
         }
+        oL += __popc(mL[i]);
+        oC += __popc(mC[i]);
+        oR += __popc(mR[i]);
         if (!ok) {
             set_status(a.status, KDT_EINTERNAL);
             side[i] = 3;
         }
     }
-    for (int c = 0; c <= k; ++c) {
-        const uint32_t *scol = c < k ? a.src_keys + (int64_t)c * N : a.src_idx;
-        uint32_t *dcol = c < k ? a.dst_keys + (int64_t)c * N : a.dst_idx;
-        uint32_t *ccol = c < k ? a.cand_keys + (int64_t)c * N : a.cand_idx;
-        uint32_t v[kEPT];
-        if (c == d) {
+    // stores: preloaded words first, then (k > kPre) the remaining columns,
+    // each with its loads issued ahead of its stores
 #pragma unroll
-            for (int i = 0; i < kEPT; ++i) v[i] = key[i];
-        } else {
+    for (int c = 0; c <= kPre; ++c) {
+        if (c < kPre && c >= k) continue;
+        uint32_t *dcol = c == kPre ? a.dst_idx : a.dst_keys + (int64_t)c * N;
+        uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * N;
 #pragma unroll
-            for (int i = 0; i < kEPT; ++i)
-                if (side[i] != 3) v[i] = __ldg(scol + t0 + (int64_t)i * nt + tid);
+        for (int i = 0; i < kEPT; ++i) {
+            if (side[i] == 3) continue;
+            (side[i] == 1 ? ccol : dcol)[pos[i]] = pv[c][i];
+            if (fh != nullptr && c == dn && side[i] != 1)
+                atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
         }
+    }
+    for (int c = kPre; c < k; ++c) {
+        const uint32_t *scol = a.src_keys + (int64_t)c * N;
+        uint32_t *dcol = a.dst_keys + (int64_t)c * N;
+        uint32_t *ccol = a.cand_keys + (int64_t)c * N;
+        uint32_t v[kEPT];
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i)
+            if (side[i] != 3) v[i] = __ldg(scol + t0 + (int64_t)i * nt + tid);
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 3) continue;
@@ -471,8 +534,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
 }
 
 __global__ void __launch_bounds__(kLvlThreads, 2) level_part_kernel(LevelArgs a) {
-    __shared__ unsigned long long red64[32];
-    __shared__ uint32_t bases[3];
+    __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
     if (stop_requested(a.status, &stop)) return;
@@ -496,7 +558,7 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_part_kernel(LevelArgs a)
         }
         __syncthreads();
         for (int64_t t0 = p; t0 < pe; t0 += kTile)
-            part_tile(a, g, bk, pp, t0, pe, &a.sel[g.j].curL, red64, bases, fuse ? fh : nullptr, bkc, dn);
+            part_tile(a, g, bk, pp, t0, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         __syncthreads();
         if (fuse) {
             uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
@@ -533,8 +595,7 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) 
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t red[64];
-    __shared__ unsigned long long red64[32];
-    __shared__ uint32_t bases[3];
+    __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
     __shared__ uint32_t cursors[3];
     __shared__ uint32_t medw[kMaxWords];
     __shared__ uint32_t cur2[2];
@@ -562,7 +623,7 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) 
     none.lo = 0.f;
     none.scale = 0.f;
     for (int64_t t0 = g.base; t0 < g.base + (int64_t)g.n; t0 += kTile)
-        part_tile(a, g, bk, pp, t0, g.base + (int64_t)g.n, cursors, red64, bases, nullptr, none, 0);
+        part_tile(a, g, bk, pp, t0, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
     __syncthreads();
     if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
