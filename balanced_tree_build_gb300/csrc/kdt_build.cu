@@ -34,7 +34,7 @@ constexpr int kInitThreads = 256;
 constexpr int kInitPPT = 4;  // points per thread per iteration
 
 __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restrict__ pts, int64_t N,
-                                                            int k, uint32_t *__restrict__ keys,
+                                                            int k, int64_t ld, uint32_t *__restrict__ keys,
                                                             uint32_t *__restrict__ idx,
                                                             uint32_t *__restrict__ bbox,
                                                             int *__restrict__ status) {
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
                     if (i < N) {
                         bad |= !isfinite(f[u]);
                         const uint32_t key = f2key(f[u]);
-                        keys[(int64_t)c * N + i] = key;
+                        keys[(int64_t)c * ld + i] = key;
                         mn[c] = min(mn[c], key);
                         mx[c] = max(mx[c], key);
                     }
@@ -128,8 +128,9 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     off = align_up(off + 64, 256);
     q.off_bbox = off;
     off = align_up(off + (size_t)2 * k * 4, 256);
+    q.ld = (N + 7) & ~(int64_t)7;
     for (int b = 0; b < 3; ++b) {
-        const int64_t rows = (b < 2 || lf > 0) ? N : 0;
+        const int64_t rows = (b < 2 || lf > 0) ? q.ld : 0;
         q.off_keys[b] = off;
         off = align_up(off + (size_t)k * rows * 4, 256);
         q.off_idx[b] = off;
@@ -189,7 +190,7 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 16;
         if (blocks > cap) blocks = cap;
         ProfScope ps(stream, "init", 0.0);
-        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, b.keys[0], b.idx[0], b.bbox,
+        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], b.idx[0], b.bbox,
                                                                    b.status);
         KDT_LAUNCH_CHECK();
     }

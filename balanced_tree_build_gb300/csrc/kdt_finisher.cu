@@ -15,7 +15,7 @@
 //     and ranks the few points of the split bucket exactly;
 //   * phase B (nodes <= 256): each warp owns whole subtrees; nodes > 32 are
 //     split the same way by one warp, nodes <= 32 rank their points with one
-//     lane per point, subtrees of <= 7 points are finished by one lane each.
+//     lane per point, subtrees of <= 15 points are finished by one lane each.
 // Phase-B subtrees are laid out relative to the range the warp took over, so
 // warps never touch each other's ranges.
 #include "kdt_internal.cuh"
@@ -26,7 +26,7 @@ namespace kdt {
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kWarpMax = 256;  // phase B: subtrees this small go to one warp
-constexpr int kLaneMax = 7;    // subtrees this small go to one lane
+constexpr int kLaneMax = 15;   // subtrees this small go to one lane
 constexpr int kCandPerWarp = 64;  // bucket-split candidates per warp
 constexpr size_t kFinSmemBudget = 200 * 1024;
 constexpr int kFinHistWords = kFinWarps * kWarpRadixBins;  // 4096
@@ -34,6 +34,7 @@ constexpr int kFinHistWords = kFinWarps * kWarpRadixBins;  // 4096
 struct FinArgs {
     Shape S;
     int k, mode, l0, T;
+    int64_t ld;
     const uint32_t *src_keys, *src_idx;
     int32_t *perm;
     const float *dom;  // node table of level l0
@@ -154,14 +155,18 @@ struct NodeGeom {
 __device__ __forceinline__ NodeGeom node_geom(const Shape &S, int64_t root, int jr, uint32_t off_root, int j,
                                               int64_t u) {
     NodeGeom g;
-    g.n = (uint32_t)seg_size(S, j, u);
-    g.off = off_root + (uint32_t)(seg_begin(S, j, u) - seg_begin(S, j, ((root + 1) << (j - jr)) - 1));
+    const int32_t u32 = (int32_t)u;
+    const int32_t first_j = (int32_t)(((root + 1) << (j - jr)) - 1);
+    g.n = (uint32_t)seg_size32(S, j, u32);
+    g.off = off_root + (uint32_t)(seg_begin32(S, j, u32) - seg_begin32(S, j, first_j));
     g.children = j + 1 < S.L;
-    g.m = g.children ? (uint32_t)seg_size(S, j + 1, 2 * u + 1) : 0u;
-    g.left_off = 0;
-    if (g.children)
-        g.left_off = off_root + (uint32_t)(seg_begin(S, j + 1, 2 * u + 1) -
-                                           seg_begin(S, j + 1, ((root + 1) << (j + 1 - jr)) - 1));
+    g.m = 0u;
+    g.left_off = 0u;
+    if (g.children && g.n > 1u) {
+        const int32_t first_j1 = 2 * first_j + 1;
+        g.m = (uint32_t)seg_size32(S, j + 1, 2 * u32 + 1);
+        g.left_off = off_root + (uint32_t)(seg_begin32(S, j + 1, 2 * u32 + 1) - seg_begin32(S, j + 1, first_j1));
+    }
     g.right_off = g.left_off + g.m;
     return g;
 }
@@ -427,26 +432,23 @@ __device__ void warp_split_small(const FinArgs &a, const FinSmem &sm, int64_t s0
 }
 
 // One lane finishes the whole subtree of node u (level j, at most kLaneMax
-// points at ids[off..off+n)): sort by the split order, take the split rank,
-// recurse on the sides (explicit stack).
-__device__ void lane_finish(const FinArgs &a, const FinSmem &sm, int64_t s0, int j, int64_t u, const uint16_t *ids,
+// points at ids[0..n)): sort them in place by the split order, take the split
+// rank, recurse on the two sides (explicit stack).
+__device__ void lane_finish(const FinArgs &a, const FinSmem &sm, int64_t s0, int j, int64_t u, uint16_t *e,
                             uint32_t n) {
     const int k = a.k, T = a.T;
-    uint32_t e[kLaneMax];
-    for (uint32_t i = 0; i < n; ++i) e[i] = ids[i];
     struct Item {
-        int64_t u;
-        int j;
-        uint8_t lo, n;
+        int32_t u;
+        int8_t j, lo, n;
     };
-    Item stack[kLaneMax];
+    Item stack[8];
     int sp = 0;
-    stack[sp++] = Item{u, j, 0, (uint8_t)n};
+    stack[sp++] = Item{(int32_t)u, (int8_t)(j - a.l0), 0, (int8_t)n};
     while (sp > 0) {
         const Item it = stack[--sp];
         if (it.n == 0) continue;
-        const int d = fin_dim(a, sm, s0, it.j, it.u);
-        // insertion sort of e[lo .. lo+n) by the split order of d
+        const int jj = a.l0 + it.j;
+        const int d = fin_dim(a, sm, s0, jj, it.u);
         for (int x = it.lo + 1; x < it.lo + it.n; ++x) {
             const uint32_t v = e[x];
             int y = x - 1;
@@ -454,15 +456,15 @@ __device__ void lane_finish(const FinArgs &a, const FinSmem &sm, int64_t s0, int
                 e[y + 1] = e[y];
                 --y;
             }
-            e[y + 1] = v;
+            e[y + 1] = (uint16_t)v;
         }
-        const uint32_t m = it.j + 1 < a.S.L ? (uint32_t)seg_size(a.S, it.j + 1, 2 * it.u + 1) : 0u;
+        const uint32_t m = (jj + 1 < a.S.L && it.n > 1) ? (uint32_t)seg_size32(a.S, jj + 1, 2 * it.u + 1) : 0u;
         const uint32_t med = e[it.lo + m];
         a.perm[it.u] = (int32_t)sm.idx[med];
-        record_split(a, sm, s0, it.j, it.u, med, d);
+        record_split(a, sm, s0, jj, it.u, med, d);
         if (it.n > 1) {
-            stack[sp++] = Item{2 * it.u + 2, it.j + 1, (uint8_t)(it.lo + m + 1), (uint8_t)(it.n - m - 1)};
-            stack[sp++] = Item{2 * it.u + 1, it.j + 1, it.lo, (uint8_t)m};
+            stack[sp++] = Item{2 * it.u + 2, (int8_t)(it.j + 1), (int8_t)(it.lo + m + 1), (int8_t)(it.n - m - 1)};
+            stack[sp++] = Item{2 * it.u + 1, (int8_t)(it.j + 1), it.lo, (int8_t)m};
         }
     }
 }
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
         return;
     }
     for (int c = 0; c < k; ++c)
-        for (uint32_t q = tid; q < n; q += blockDim.x) sm.keys[c * a.T + q] = a.src_keys[(int64_t)c * N + base + q];
+        for (uint32_t q = tid; q < n; q += blockDim.x) sm.keys[c * a.T + q] = a.src_keys[(int64_t)c * a.ld + base + q];
     for (uint32_t q = tid; q < n; q += blockDim.x) {
         sm.idx[q] = a.src_idx[base + q];
         sm.ids[0][q] = (uint16_t)q;
@@ -592,6 +594,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.mode = p.mode;
     a.l0 = p.finish_level;
     a.T = p.tp.tile;
+    a.ld = p.ld;
     a.src_keys = b.keys[src];
     a.src_idx = b.idx[src];
     a.perm = perm;

@@ -74,6 +74,24 @@ __host__ __device__ __forceinline__ int64_t seg_begin(const Shape &S, int l, int
     return full_nodes(l) + j * A + (t < S.M ? t : S.M);
 }
 
+// 32-bit forms of ss and sb for device code: with N < 2^31 every node id,
+// size and position fits; requires l < L and s on level l.
+__device__ __forceinline__ int32_t seg_size32(const Shape &S, int l, int32_t s) {
+    if (s >= (int32_t)S.N) return 0;
+    const int32_t B = 1 << (S.L - 1 - l);
+    const int32_t j = s - ((1 << l) - 1);
+    int32_t r = (int32_t)S.M - j * B;
+    r = r < 0 ? 0 : (r > B ? B : r);
+    return B - 1 + r;
+}
+
+__device__ __forceinline__ int32_t seg_begin32(const Shape &S, int l, int32_t s) {
+    const int32_t B = 1 << (S.L - 1 - l);
+    const int32_t j = s - ((1 << l) - 1);
+    const int32_t t = j * B;
+    return ((1 << l) - 1) + j * (B - 1) + (t < (int32_t)S.M ? t : (int32_t)S.M);
+}
+
 // Number of nodes that exist on level l.
 __host__ __device__ __forceinline__ int64_t nodes_on_level(const Shape &S, int l) {
     const int64_t w = (int64_t)1 << l;
@@ -145,6 +163,7 @@ struct Plan {
     int64_t table_cap;   // node-table entries per level
     int64_t hist_rows;   // histogram rows per buffer (multi-CTA levels)
     int64_t sel_cap;     // SegSel entries
+    int64_t ld;          // column stride of the record buffers (N rounded up to 8)
     // byte offsets inside the workspace
     size_t off_status, off_bbox, off_keys[3], off_idx[3], off_dom[2], off_dim[2], off_hist[2], off_sel;
     size_t bytes;

@@ -33,9 +33,10 @@ namespace kdt {
 
 constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
-constexpr int kEPT = 4;                          // points per thread per tile
+constexpr int kEPT = 8;                          // consecutive points per thread per tile
+constexpr int kPartThreads = 256;                // partition CTAs (multi-CTA and per-subtree)
 constexpr int kPre = 4;                          // key columns loaded ahead in a tile
-constexpr int kTile = kLvlThreads * kEPT;
+constexpr int kTile = kPartThreads * kEPT;
 
 // ---- value buckets ----------------------------------------------------------
 
@@ -101,6 +102,7 @@ struct LevelArgs {
     SegSel *sel;
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
+    int64_t ld;          // column stride of the record buffers
 };
 
 struct SegInfo {
@@ -203,49 +205,72 @@ __device__ __forceinline__ int64_t cand_pos(const SegInfo &g, const PartPlan &pp
     return slot + 1u < pp.cnt ? g.left_begin + pp.below + slot : g.s;
 }
 
+// Loads the 8 consecutive words at col[q0 .. q0+8) (q0 a multiple of 8) as
+// two 128-bit loads.
+__device__ __forceinline__ void load8(const uint32_t *col, int64_t q0, uint32_t *v) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(col + q0);
+    const uint4 x = __ldg(p), y = __ldg(p + 1);
+    v[0] = x.x;
+    v[1] = x.y;
+    v[2] = x.z;
+    v[3] = x.w;
+    v[4] = y.x;
+    v[5] = y.y;
+    v[6] = y.z;
+    v[7] = y.w;
+}
+
+// Partitions the points of [vb, ve) that fall in the tile starting at t0 (a
+// multiple of 8): thread t handles positions t0 + 8t .. t0 + 8t + 7.
 // `cursors` points at three counters (left, candidate, right) in shared or
 // global memory; `wtot` and `wbase` are 3 words per warp of shared scratch;
 // `fh` is the fused children's histogram in shared memory, or null.
 //
-// Output order is slot-major per warp: for each of a thread's kEPT points the
-// warp's lanes going to one side write consecutive positions (ballot +
-// popcount), so every warp store covers one contiguous run.
+// Every word of the thread's records that fits the register budget is
+// loaded first (128-bit loads), so a thread waits for about one memory
+// latency per tile.  Output order is slot-major per warp: for each of the 8
+// slots the warp's lanes going to one side write consecutive positions
+// (ballot + popcount), so every warp store covers one contiguous run.
 __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
-                          int64_t pe, uint32_t *cursors, uint32_t *wtot, uint32_t *wbase, uint32_t *fh,
+                          int64_t vb, int64_t ve, uint32_t *cursors, uint32_t *wtot, uint32_t *wbase, uint32_t *fh,
                           const Bucketer &bkc, int dn) {
-    const int64_t N = a.S.N;
+    const int64_t ld = a.ld;
     const int k = a.k, d = g.d;
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    // Every word of the tile's records that fits the register budget is
-    // loaded here, before the reservation, so a thread waits for about one
-    // memory latency per tile: [c][i] holds key column c (c < kPre) and, at
-    // c = kPre, the input index.
+    const int64_t q0 = t0 + 8 * (int64_t)tid;
+    const bool any = q0 + 8 > vb && q0 < ve;
     uint32_t pv[kPre + 1][kEPT];
-    uint32_t mL[kEPT], mR[kEPT], mC[kEPT];
-    uint32_t tL = 0, tC = 0, tR = 0;
 #pragma unroll
-    for (int i = 0; i < kEPT; ++i) {
-        const int64_t q = t0 + (int64_t)i * nt + tid;
-        const bool valid = q < pe;
+    for (int c = 0; c <= kPre; ++c) {
 #pragma unroll
-        for (int c = 0; c <= kPre; ++c) {
-            pv[c][i] = 0u;
-            if (valid && (c == kPre || c < k)) pv[c][i] = __ldg((c == kPre ? a.src_idx : a.src_keys + (int64_t)c * N) + q);
-        }
+        for (int i = 0; i < kEPT; ++i) pv[c][i] = 0u;
+        if (any && (c == kPre || c < k)) load8(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
     }
+    uint32_t kx[kEPT];
+    if (d < kPre) {
 #pragma unroll
-    for (int i = 0; i < kEPT; ++i) {
-        const int64_t q = t0 + (int64_t)i * nt + tid;
-        int side = 3;
-        if (q < pe) {
+        for (int i = 0; i < kEPT; ++i) {
             uint32_t key = pv[0][i];  // static indices keep pv in registers
 #pragma unroll
             for (int c = 1; c < kPre; ++c)
                 if (d == c) key = pv[c][i];
-            if (d >= kPre) key = __ldg(a.src_keys + (int64_t)d * N + q);
-            const uint32_t b = (uint32_t)bk(key);
+            kx[i] = key;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i) kx[i] = 0u;
+        if (any) load8(a.src_keys + (int64_t)d * ld, q0, kx);
+    }
+    uint32_t mL[kEPT], mR[kEPT], mC[kEPT];
+    uint32_t tL = 0, tC = 0, tR = 0;
+#pragma unroll
+    for (int i = 0; i < kEPT; ++i) {
+        const int64_t q = q0 + i;
+        int side = 3;
+        if (q >= vb && q < ve) {
+            const uint32_t b = (uint32_t)bk(kx[i]);
             side = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
         }
         mL[i] = __ballot_sync(0xffffffffu, side == 0);
@@ -319,13 +344,12 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
             side[i] = 3;
         }
     }
-    // stores: preloaded words first, then (k > kPre) the remaining columns,
-    // each with its loads issued ahead of its stores
+    // stores: preloaded words first, then (k > kPre) the remaining columns
 #pragma unroll
     for (int c = 0; c <= kPre; ++c) {
         if (c < kPre && c >= k) continue;
-        uint32_t *dcol = c == kPre ? a.dst_idx : a.dst_keys + (int64_t)c * N;
-        uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * N;
+        uint32_t *dcol = c == kPre ? a.dst_idx : a.dst_keys + (int64_t)c * ld;
+        uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * ld;
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 3) continue;
@@ -335,13 +359,12 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         }
     }
     for (int c = kPre; c < k; ++c) {
-        const uint32_t *scol = a.src_keys + (int64_t)c * N;
-        uint32_t *dcol = a.dst_keys + (int64_t)c * N;
-        uint32_t *ccol = a.cand_keys + (int64_t)c * N;
+        uint32_t *dcol = a.dst_keys + (int64_t)c * ld;
+        uint32_t *ccol = a.cand_keys + (int64_t)c * ld;
         uint32_t v[kEPT];
 #pragma unroll
-        for (int i = 0; i < kEPT; ++i)
-            if (side[i] != 3) v[i] = __ldg(scol + t0 + (int64_t)i * nt + tid);
+        for (int i = 0; i < kEPT; ++i) v[i] = 0u;
+        if (any) load8(a.src_keys + (int64_t)c * ld, q0, v);
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 3) continue;
@@ -356,7 +379,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
 // Word i of candidate slot q (split order of dimension d).
 struct CandAcc {
     const uint32_t *keys, *idx;
-    int64_t N, gap_begin, s;
+    int64_t ld, gap_begin, s;  // ld: column stride
     uint32_t cnt;
     int k, d;
     __device__ __forceinline__ int64_t pos(uint32_t q) const { return q + 1u < cnt ? gap_begin + q : s; }
@@ -365,7 +388,7 @@ struct CandAcc {
         if (i == k) return idx[p];
         int c = d + i;
         if (c >= k) c -= k;
-        return keys[(int64_t)c * N + p];
+        return keys[(int64_t)c * ld + p];
     }
 };
 
@@ -377,9 +400,9 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
                                 uint32_t *hist, uint32_t *red, uint32_t *medw, uint32_t *cur2, bool fuse, int dn) {
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const int k = a.k;
-    const int64_t N = a.S.N;
+    const int64_t ld = a.ld;
     const uint32_t r = g.m - pp.below;  // rank of the split point among the candidates
-    const CandAcc acc{a.cand_keys, a.cand_idx, N, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
+    const CandAcc acc{a.cand_keys, a.cand_idx, ld, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
     cta_select(acc, pp.cnt, r, k + 1, st, hist, red);
     if (st.err) {
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
@@ -426,8 +449,8 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
             if (ok) {
                 const int64_t sp = acc.pos(q);
                 for (int c = 0; c < k; ++c) {
-                    const uint32_t v = a.cand_keys[(int64_t)c * N + sp];
-                    a.dst_keys[(int64_t)c * N + pos] = v;
+                    const uint32_t v = a.cand_keys[(int64_t)c * ld + sp];
+                    a.dst_keys[(int64_t)c * ld + pos] = v;
                     if (fuse && c == dn)
                         atomicAdd(&a.hist_nxt[(2 * g.j + side) * kBuckets + bkc(v)], 1u);
                 }
@@ -481,7 +504,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
     if (stop_requested(a.status, &stop)) return;
     const int64_t begin = full_nodes(a.l) + (int64_t)blockIdx.x * a.per_cta;
     const int64_t end = min(a.S.N, begin + a.per_cta);
-    const int64_t N = a.S.N;
+    const int64_t ld = a.ld;
     for (int64_t p = begin; p < end;) {
         const int64_t s = seg_of_pos(a.S, a.l, p);
         const SegInfo g = seg_info(a, s);
@@ -489,7 +512,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
         const Bucketer bk = seg_bucketer(a, g.j, g.d);
         for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        const uint32_t *col = a.src_keys + (int64_t)g.d * N;
+        const uint32_t *col = a.src_keys + (int64_t)g.d * ld;
         for (int64_t q = p + threadIdx.x; q < pe; q += blockDim.x) atomicAdd(&hist[bk(col[q])], 1u);
         __syncthreads();
         uint32_t *H = a.hist_cur + g.j * kBuckets;
@@ -533,7 +556,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
     return pp;
 }
 
-__global__ void __launch_bounds__(kLvlThreads, 2) level_part_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 2) level_part_kernel(LevelArgs a) {
     __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
@@ -557,8 +580,8 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_part_kernel(LevelArgs a)
             for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
         }
         __syncthreads();
-        for (int64_t t0 = p; t0 < pe; t0 += kTile)
-            part_tile(a, g, bk, pp, t0, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
+        for (int64_t t0 = p & ~(int64_t)7; t0 < pe; t0 += kTile)
+            part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         __syncthreads();
         if (fuse) {
             uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
@@ -591,7 +614,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
 
 // ---- one CTA per subtree -------------------------------------------------------
 
-__global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 2) level_seg_kernel(LevelArgs a) {
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t red[64];
@@ -605,8 +628,8 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) 
     const int64_t s = full_nodes(a.l) + blockIdx.x;
     const SegInfo g = seg_info(a, s);
     const Bucketer bk = seg_bucketer(a, g.j, g.d);
-    const int64_t N = a.S.N;
-    const uint32_t *col = a.src_keys + (int64_t)g.d * N;
+    const int64_t ld = a.ld;
+    const uint32_t *col = a.src_keys + (int64_t)g.d * ld;
     for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
     if (threadIdx.x < 3) cursors[threadIdx.x] = 0u;
     __syncthreads();
@@ -622,8 +645,8 @@ __global__ void __launch_bounds__(kLvlThreads, 2) level_seg_kernel(LevelArgs a) 
     Bucketer none;
     none.lo = 0.f;
     none.scale = 0.f;
-    for (int64_t t0 = g.base; t0 < g.base + (int64_t)g.n; t0 += kTile)
-        part_tile(a, g, bk, pp, t0, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
+    for (int64_t t0 = g.base & ~(int64_t)7; t0 < g.base + (int64_t)g.n; t0 += kTile)
+        part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
     __syncthreads();
     if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
@@ -658,6 +681,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.sel = b.sel;
     a.status = b.status;
     a.per_cta = 0;
+    a.ld = p.ld;
     const int64_t nseg = nodes_on_level(S, l);
     const int64_t live = S.N - full_nodes(l);
     const double alg = 20.0 * (double)live;
@@ -667,7 +691,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        const int64_t grid = (int64_t)sms * 3;
+        const int64_t grid = (int64_t)sms * 2;  // two partition CTAs per SM stay resident
         a.per_cta = (live + grid - 1) / grid;
         const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
         const bool fused_here = l > 0 && fusable;
@@ -685,7 +709,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         }
         {
             ProfScope ps(stream, "part", alg);
-            level_part_kernel<<<(unsigned)nblk, kLvlThreads, 0, stream>>>(a);
+            level_part_kernel<<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         {
@@ -695,7 +719,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         }
     } else {
         ProfScope ps(stream, "seg", alg);
-        level_seg_kernel<<<(unsigned)nseg, kLvlThreads, 0, stream>>>(a);
+        level_seg_kernel<<<(unsigned)nseg, kPartThreads, 0, stream>>>(a);
         if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
     }
     return KDT_OK;
