@@ -128,7 +128,7 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     off = align_up(off + 64, 256);
     q.off_bbox = off;
     off = align_up(off + (size_t)2 * k * 4, 256);
-    q.ld = (N + 7) & ~(int64_t)7;
+    q.ld = (N + 7) & ~(int64_t)7;  // multiple of 4 words: 128-bit loads stay aligned
     for (int b = 0; b < 3; ++b) {
         const int64_t rows = (b < 2 || lf > 0) ? q.ld : 0;
         q.off_keys[b] = off;

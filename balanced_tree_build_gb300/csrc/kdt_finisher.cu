@@ -493,12 +493,21 @@ __global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    for (int c = 0; c < k; ++c)
-        for (uint32_t q = tid; q < n; q += blockDim.x) sm.keys[c * a.T + q] = a.src_keys[(int64_t)c * a.ld + base + q];
-    for (uint32_t q = tid; q < n; q += blockDim.x) {
-        sm.idx[q] = a.src_idx[base + q];
-        sm.ids[0][q] = (uint16_t)q;
+    // load the tile: all loads of a batch are issued before its stores
+    for (int c = 0; c <= k; ++c) {
+        const uint32_t *col = (c < k ? a.src_keys + (int64_t)c * a.ld : a.src_idx) + base;
+        uint32_t *dstc = c < k ? sm.keys + c * a.T : sm.idx;
+        const uint32_t nt = blockDim.x;
+        for (uint32_t q = tid; q < n; q += 4 * nt) {
+            uint32_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = q + u * nt < n ? __ldg(col + q + u * nt) : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q + u * nt < n) dstc[q + u * nt] = v[u];
+        }
     }
+    for (uint32_t q = tid; q < n; q += blockDim.x) sm.ids[0][q] = (uint16_t)q;
     __syncthreads();
 
     const uint32_t w = tid >> 5;
@@ -594,6 +603,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.mode = p.mode;
     a.l0 = p.finish_level;
     a.T = p.tp.tile;
+    a.ld = p.ld;
     a.ld = p.ld;
     a.src_keys = b.keys[src];
     a.src_idx = b.idx[src];

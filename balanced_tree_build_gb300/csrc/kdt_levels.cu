@@ -33,7 +33,7 @@ namespace kdt {
 
 constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
-constexpr int kEPT = 8;                          // consecutive points per thread per tile
+constexpr int kEPT = 4;                          // consecutive points per thread per tile
 constexpr int kPartThreads = 256;                // partition CTAs (multi-CTA and per-subtree)
 constexpr int kPre = 4;                          // key columns loaded ahead in a tile
 constexpr int kTile = kPartThreads * kEPT;
@@ -205,30 +205,25 @@ __device__ __forceinline__ int64_t cand_pos(const SegInfo &g, const PartPlan &pp
     return slot + 1u < pp.cnt ? g.left_begin + pp.below + slot : g.s;
 }
 
-// Loads the 8 consecutive words at col[q0 .. q0+8) (q0 a multiple of 8) as
-// two 128-bit loads.
-__device__ __forceinline__ void load8(const uint32_t *col, int64_t q0, uint32_t *v) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(col + q0);
-    const uint4 x = __ldg(p), y = __ldg(p + 1);
+// Loads the 4 consecutive words at col[q0 .. q0+4) (q0 a multiple of 4) as
+// one 128-bit load.
+__device__ __forceinline__ void load4(const uint32_t *col, int64_t q0, uint32_t *v) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(col + q0));
     v[0] = x.x;
     v[1] = x.y;
     v[2] = x.z;
     v[3] = x.w;
-    v[4] = y.x;
-    v[5] = y.y;
-    v[6] = y.z;
-    v[7] = y.w;
 }
 
 // Partitions the points of [vb, ve) that fall in the tile starting at t0 (a
-// multiple of 8): thread t handles positions t0 + 8t .. t0 + 8t + 7.
+// multiple of 4): thread t handles positions t0 + 4t .. t0 + 4t + 3.
 // `cursors` points at three counters (left, candidate, right) in shared or
 // global memory; `wtot` and `wbase` are 3 words per warp of shared scratch;
 // `fh` is the fused children's histogram in shared memory, or null.
 //
 // Every word of the thread's records that fits the register budget is
 // loaded first (128-bit loads), so a thread waits for about one memory
-// latency per tile.  Output order is slot-major per warp: for each of the 8
+// latency per tile.  Output order is slot-major per warp: for each of the 4
 // slots the warp's lanes going to one side write consecutive positions
 // (ballot + popcount), so every warp store covers one contiguous run.
 __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
@@ -239,14 +234,14 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    const int64_t q0 = t0 + 8 * (int64_t)tid;
-    const bool any = q0 + 8 > vb && q0 < ve;
+    const int64_t q0 = t0 + 4 * (int64_t)tid;
+    const bool any = q0 + 4 > vb && q0 < ve;
     uint32_t pv[kPre + 1][kEPT];
 #pragma unroll
     for (int c = 0; c <= kPre; ++c) {
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) pv[c][i] = 0u;
-        if (any && (c == kPre || c < k)) load8(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
+        if (any && (c == kPre || c < k)) load4(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
     }
     uint32_t kx[kEPT];
     if (d < kPre) {
@@ -261,7 +256,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     } else {
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) kx[i] = 0u;
-        if (any) load8(a.src_keys + (int64_t)d * ld, q0, kx);
+        if (any) load4(a.src_keys + (int64_t)d * ld, q0, kx);
     }
     uint32_t mL[kEPT], mR[kEPT], mC[kEPT];
     uint32_t tL = 0, tC = 0, tR = 0;
@@ -364,7 +359,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         uint32_t v[kEPT];
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) v[i] = 0u;
-        if (any) load8(a.src_keys + (int64_t)c * ld, q0, v);
+        if (any) load4(a.src_keys + (int64_t)c * ld, q0, v);
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 3) continue;
@@ -556,7 +551,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
     return pp;
 }
 
-__global__ void __launch_bounds__(kPartThreads, 2) level_part_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 4) level_part_kernel(LevelArgs a) {
     __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
@@ -580,7 +575,7 @@ __global__ void __launch_bounds__(kPartThreads, 2) level_part_kernel(LevelArgs a
             for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
         }
         __syncthreads();
-        for (int64_t t0 = p & ~(int64_t)7; t0 < pe; t0 += kTile)
+        for (int64_t t0 = p & ~(int64_t)3; t0 < pe; t0 += kTile)
             part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         __syncthreads();
         if (fuse) {
@@ -614,7 +609,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
 
 // ---- one CTA per subtree -------------------------------------------------------
 
-__global__ void __launch_bounds__(kPartThreads, 2) level_seg_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 4) level_seg_kernel(LevelArgs a) {
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t red[64];
@@ -645,7 +640,7 @@ __global__ void __launch_bounds__(kPartThreads, 2) level_seg_kernel(LevelArgs a)
     Bucketer none;
     none.lo = 0.f;
     none.scale = 0.f;
-    for (int64_t t0 = g.base & ~(int64_t)7; t0 < g.base + (int64_t)g.n; t0 += kTile)
+    for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile)
         part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
     __syncthreads();
     if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
@@ -691,7 +686,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        const int64_t grid = (int64_t)sms * 2;  // two partition CTAs per SM stay resident
+        const int64_t grid = (int64_t)sms * 4;  // four partition CTAs per SM stay resident
         a.per_cta = (live + grid - 1) / grid;
         const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
         const bool fused_here = l > 0 && fusable;
