@@ -160,6 +160,29 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from profiles/traffic_uniform_100m.txt,
+    or None if not recorded or if the kernel's source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_uniform_100m.txt")
+    try:
+        with open(path) as f:
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    for t in lines:
+        if len(t) >= 8 and t[0] == "kernel" and t[1] == kernel:
+            src, sha, nbytes = t[3], t[5], float(t[7])
+            try:
+                with open(os.path.join(ROOT, src), "rb") as f:
+                    if hashlib.sha256(f.read()).hexdigest()[:len(sha)] != sha:
+                        return None
+            except OSError:
+                return None
+            return nbytes
+    return None
+
+
 def b_alg(n: int) -> float:
     """Algorithmic bytes of the level-by-level method: per point and sort
     level 20 B (read tag, index and split coordinate; write tag and index),
@@ -296,9 +319,10 @@ def run_ours(args, workload):
         avg_ms = dom["total_ms"] / dom["launches"]
         avg_bytes = dom["bytes_alg"] / dom["launches"]
         achieved = avg_bytes / (avg_ms / 1e3) / 1e9
+        traffic = recorded_traffic(dom["name"]) if workload.name == "uniform_100m" else None
         roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                    "traffic": None, "avg_launch_ms": avg_ms, "alg_bytes_per_launch": avg_bytes}
+                    "traffic": traffic, "avg_launch_ms": avg_ms, "alg_bytes_per_launch": avg_bytes}
     balg = b_alg(n)
     build_gbs = balg / (ms_step / 1e3) / 1e9
     build_roof = {"B_alg_bytes": balg, "achieved_GBps": build_gbs, "frac_of_measured": build_gbs / peak,
@@ -354,9 +378,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-sample", type=int, default=1 << 18,
                     help="points per step for --impl reference")
+    ap.add_argument("--n", type=int, default=None,
+                    help="build a sample of this many points of the workload's distribution "
+                         "instead of the full workload (profiling runs)")
     args = ap.parse_args(argv)
-    from balanced_tree_build_gb300.inputs import WORKLOADS
+    from balanced_tree_build_gb300.inputs import WORKLOADS, Workload
     workload = WORKLOADS[args.workload]
+    if args.n is not None and args.n != workload.n:
+        w = workload
+        workload = Workload(f"{w.name}_sample{args.n}", args.n, w.k, w.mode, w.dist, w.seed)
     if args.impl == "reference":
         return run_reference(args, workload)
     return run_ours(args, workload)

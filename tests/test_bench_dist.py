@@ -52,3 +52,21 @@ def test_b_alg_model():
     assert bench.b_alg(10) == 10 * (20 * 3 + 12)
     assert bench.b_alg(100_000_000) == pytest.approx(53.2e9, rel=1e-3)
     assert bench.b_alg(1) == 12.0
+
+
+def test_recorded_traffic_tracks_kernel_source(tmp_path, monkeypatch):
+    import shutil
+    # the table in profiles/ matches the committed sources
+    for kern in ("finisher", "part"):
+        v = bench.recorded_traffic(kern)
+        assert v is None or v > 0
+    assert bench.recorded_traffic("no_such_kernel") is None
+    # a changed kernel source invalidates the recorded figure
+    root = tmp_path / "repo"
+    (root / "profiles").mkdir(parents=True)
+    shutil.copy(os.path.join(bench.ROOT, "profiles", "traffic_uniform_100m.txt"), root / "profiles")
+    src = root / "balanced_tree_build_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "kdt_finisher.cu").write_text("// changed\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.recorded_traffic("finisher") is None
