@@ -15,7 +15,7 @@
 //     and ranks the few points of the split bucket exactly;
 //   * phase B (nodes <= 256): each warp owns whole subtrees; nodes > 32 are
 //     split the same way by one warp, nodes <= 32 rank their points with one
-//     lane per point, subtrees of <= 15 points are finished by one lane each.
+//     lane per point, subtrees of <= 7 points are finished by one lane each.
 // Phase-B subtrees are laid out relative to the range the warp took over, so
 // warps never touch each other's ranges.
 #include "kdt_internal.cuh"
@@ -26,9 +26,9 @@ namespace kdt {
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kWarpMax = 256;  // phase B: subtrees this small go to one warp
-constexpr int kLaneMax = 15;   // subtrees this small go to one lane
+constexpr int kLaneMax = 7;    // subtrees this small go to one lane
 constexpr int kCandPerWarp = 64;  // bucket-split candidates per warp
-constexpr size_t kFinSmemBudget = 200 * 1024;
+constexpr size_t kFinSmemBudget = 100 * 1024;  // two CTAs per SM
 constexpr int kFinHistWords = kFinWarps * kWarpRadixBins;  // 4096
 
 struct FinArgs {
@@ -469,7 +469,7 @@ __device__ void lane_finish(const FinArgs &a, const FinSmem &sm, int64_t s0, int
     }
 }
 
-__global__ void __launch_bounds__(kFinThreads, 1) finisher_kernel(FinArgs a) {
+__global__ void __launch_bounds__(kFinThreads, 2) finisher_kernel(FinArgs a) {
     extern __shared__ __align__(16) unsigned char fin_smem[];
     __shared__ SelState st[kFinWarps];
     __shared__ uint32_t red[kFinWarps][64];
@@ -603,7 +603,6 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.mode = p.mode;
     a.l0 = p.finish_level;
     a.T = p.tp.tile;
-    a.ld = p.ld;
     a.ld = p.ld;
     a.src_keys = b.keys[src];
     a.src_idx = b.idx[src];
