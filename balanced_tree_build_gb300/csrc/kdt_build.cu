@@ -113,7 +113,7 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     q.S = make_shape(N);
     q.k = k;
     q.mode = mode;
-    if (pick_tile(k, mode, &q.tp.tile, &q.tp.smem) != 0) return KDT_EINVAL;
+    if (pick_tile(k, mode, &q.tp) != 0) return KDT_EINVAL;
     int lf = 0;
     while (lf < q.S.L && seg_size(q.S, lf, full_nodes(lf)) > q.tp.tile) ++lf;
     q.finish_level = lf;
@@ -146,6 +146,8 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     }
     q.off_sel = off;
     off = align_up(off + (size_t)q.sel_cap * sizeof(SegSel), 256);
+    q.off_fb = off;
+    off = align_up(off + (size_t)q.table_cap, 256);
     q.bytes = off;
     *p = q;
     return KDT_OK;
@@ -166,6 +168,7 @@ Buffers carve(const Plan &p, void *base) {
         r.hist[i] = reinterpret_cast<uint32_t *>(b + p.off_hist[i]);
     }
     r.sel = reinterpret_cast<SegSel *>(b + p.off_sel);
+    r.fallback = b + p.off_fb;
     return r;
 }
 

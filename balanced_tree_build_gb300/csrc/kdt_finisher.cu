@@ -1,5 +1,8 @@
-// kdt_finisher.cu -- the shared-memory finisher: one CTA owns a subtree of at
-// most T points and fixes all of its remaining levels on chip.
+// kdt_finisher.cu -- the select finisher: one CTA owns a subtree of at most T
+// points and fixes all of its remaining levels on chip by exact rank selects.
+// It runs the tiles that the sorted finisher (kdt_finisher_sorted.cu) leaves:
+// those whose coordinates fall into too few value buckets (heavy ties,
+// tightly clustered values), which its selects handle at any distribution.
 //
 // The paper's method runs every level over the whole array ("GPU-friendly,
 // Parallel, and (Almost-)In-Place Construction of Left-Balanced k-d Trees",
@@ -28,7 +31,6 @@ constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kWarpMax = 256;  // phase B: subtrees this small go to one warp
 constexpr int kLaneMax = 7;    // subtrees this small go to one lane
 constexpr int kCandPerWarp = 64;  // bucket-split candidates per warp
-constexpr size_t kFinSmemBudget = 100 * 1024;  // two CTAs per SM
 constexpr int kFinHistWords = kFinWarps * kWarpRadixBins;  // 4096
 
 struct FinArgs {
@@ -38,10 +40,11 @@ struct FinArgs {
     const uint32_t *src_keys, *src_idx;
     int32_t *perm;
     const float *dom;  // node table of level l0
+    const uint8_t *only;  // per tile: nonzero = finish it here
     int *status;
 };
 
-size_t finisher_smem_bytes(int k, int T, int mode) {
+size_t select_finisher_smem(int k, int T, int mode) {
     size_t b = (size_t)k * T * 4 + (size_t)T * 4 + (size_t)T * 4 + (size_t)kFinHistWords * 4;
     if (mode == KDT_SPLIT_WIDEST) b += (size_t)T * 5;
     return (b + 15) & ~(size_t)15;
@@ -478,6 +481,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) finisher_kernel(FinArgs a) {
     __shared__ uint16_t cand[kFinWarps * kCandPerWarp];
     __shared__ int stop;
     const uint32_t tid = threadIdx.x;
+    if (a.only != nullptr && a.only[blockIdx.x] == 0) return;
     if (tid == 0) stop = *(volatile int *)a.status;
     __syncthreads();
     if (stop) return;
@@ -582,20 +586,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) finisher_kernel(FinArgs a) {
     }
 }
 
-int pick_tile(int k, int mode, int *T, size_t *smem) {
-    static const int cands[] = {8192, 6144, 4096, 3072, 2048, 1024, 512};
-    for (int c : cands) {
-        const size_t b = finisher_smem_bytes(k, c, mode);
-        if (b <= kFinSmemBudget) {
-            *T = c;
-            *smem = b;
-            return 0;
-        }
-    }
-    return -1;
-}
-
-int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream) {
+int launch_select_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, const uint8_t *only,
+                           cudaStream_t stream) {
     const Shape &S = p.S;
     FinArgs a;
     a.S = S;
@@ -608,15 +600,13 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.src_idx = b.idx[src];
     a.perm = perm;
     a.dom = b.dom[p.finish_level & 1];
+    a.only = only;
     a.status = b.status;
-    if (cudaFuncSetAttribute(finisher_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.tp.smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(finisher_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)p.tp.smem_select) != cudaSuccess)
         return KDT_ECUDA;
     const int64_t ntiles = nodes_on_level(S, p.finish_level);
-    const double Nd = (double)S.N;
-    const double sort_levels = (double)(S.L - 1 - p.finish_level);
-    ProfScope ps(stream, "finisher", 20.0 * (Nd - (double)full_nodes(p.finish_level)) * sort_levels + 12.0 * Nd);
-    finisher_kernel<<<(unsigned)ntiles, kFinThreads, p.tp.smem, stream>>>(a);
+    finisher_kernel<<<(unsigned)ntiles, kFinThreads, p.tp.smem_select, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
     return KDT_OK;
 }

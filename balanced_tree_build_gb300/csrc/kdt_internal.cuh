@@ -138,9 +138,13 @@ __device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(st
 // Finisher tile limits: a subtree whose point count is at most `tile` is
 // finished inside one CTA's shared memory.
 struct TilePlan {
-    int tile;          // T: max points per finisher CTA
-    size_t smem;       // dynamic shared memory per finisher CTA
+    int tile;           // T: max points per finisher CTA
+    int nb;             // value buckets of the sorted finisher's counting sort
+    size_t smem;        // dynamic shared memory per sorted-finisher CTA
+    size_t smem_select; // dynamic shared memory per select-finisher CTA
 };
+
+constexpr size_t kSelectSmemMax = 200 * 1024;  // select finisher: at least one CTA per SM
 
 // Per live subtree of a global level: the value bucket that holds the split
 // rank, the point counts below it and in it, and the partition cursors.
@@ -165,7 +169,7 @@ struct Plan {
     int64_t sel_cap;     // SegSel entries
     int64_t ld;          // column stride of the record buffers (N rounded up to 8)
     // byte offsets inside the workspace
-    size_t off_status, off_bbox, off_keys[3], off_idx[3], off_dom[2], off_dim[2], off_hist[2], off_sel;
+    size_t off_status, off_bbox, off_keys[3], off_idx[3], off_dom[2], off_dim[2], off_hist[2], off_sel, off_fb;
     size_t bytes;
 };
 
@@ -180,13 +184,20 @@ struct Buffers {
     int *dim[2];
     uint32_t *hist[2];  // [rows][kBuckets]
     SegSel *sel;
+    uint8_t *fallback;  // [tiles]: 1 = tile left to the select finisher
 };
 
 Buffers carve(const Plan &p, void *base);
 
-// Finisher tile choice and launch (kdt_finisher.cu).
-int pick_tile(int k, int mode, int *T, size_t *smem);
+// Finisher tile choice and launch (kdt_finisher_sorted.cu): the sorted
+// finisher runs every tile; tiles it leaves (flag set in Buffers::fallback)
+// go to the select finisher (kdt_finisher.cu).
+int pick_tile(int k, int mode, TilePlan *tp);
 int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream);
+size_t select_finisher_smem(int k, int T, int mode);
+// Select finisher over the tiles whose flag in `only` is nonzero.
+int launch_select_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, const uint8_t *only,
+                           cudaStream_t stream);
 
 // Enqueues one global level l (records move from buffer src to src^1).
 int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm, cudaStream_t stream);
