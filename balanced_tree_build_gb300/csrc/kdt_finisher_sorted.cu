@@ -73,10 +73,10 @@ static size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Dynamic shared memory of one CTA: reference arrays [k][T] u16, keys [k][T]
 // u32 (after the sort: the second reference array set and the side flags),
-// input indices [T], nb bucket counters, a [T] u16 bucket staging array, and
+// input indices [T], nb 16-bit bucket counters, a [T] u16 bucket staging array, and
 // in widest mode the split value and dimension of every tile node.
 size_t sorted_finisher_smem(int k, int T, int mode, int nb) {
-    size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)4 * nb + (size_t)2 * T;
+    size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)2 * nb + (size_t)2 * T;
     if (mode == KDT_SPLIT_WIDEST) b += (size_t)5 * T;
     return align16(b);
 }
@@ -87,7 +87,7 @@ struct SfSmem {
     uint16_t *ids1;   // [k][T], aliases keys after the sort
     uint8_t *side;    // [T], aliases keys + 2kT bytes after the sort
     uint32_t *idx;    // [T]
-    uint32_t *hist;   // [nb]
+    uint32_t *hist;   // [nb / 2]: two 16-bit bucket counters per word
     uint16_t *stage;  // [T] points grouped by bucket, before ranking
     float *sval;      // [T] split value of tile node (widest mode)
     uint8_t *sdim;    // [T] split dimension of tile node (widest mode)
@@ -104,7 +104,7 @@ __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int n
     f.idx = reinterpret_cast<uint32_t *>(p);
     p += (size_t)4 * T;
     f.hist = reinterpret_cast<uint32_t *>(p);
-    p += (size_t)4 * nb;
+    p += (size_t)2 * nb;
     f.stage = reinterpret_cast<uint16_t *>(p);
     p += (size_t)2 * T;
     f.sval = reinterpret_cast<float *>(p);
@@ -299,6 +299,8 @@ __device__ void sf_finish_small(const SfArgs &a, const SfSmem &sm, int64_t s0, i
     }
     for (int32_t q = 0; q < nn; ++q) code[A[o + q] & tmask] = 0;
     uint32_t done = 0u;  // local nodes already emitted by their parent
+    const int32_t M = (int32_t)S.M;
+    const int d0 = j % k;
     for (int v = 0; v < 15; ++v) {
         if ((done >> v) & 1u) continue;
         const int lev = 31 - __clz(v + 1);
@@ -306,11 +308,20 @@ __device__ void sf_finish_small(const SfArgs &a, const SfSmem &sm, int64_t s0, i
         if (jj >= S.L) break;
         const int32_t vl = v + 1 - (1 << lev);
         const int64_t uv = ((u + 1) << lev) - 1 + vl;
-        const int32_t nv = (int32_t)seg_size(S, jj, uv);
-        if (nv == 0) continue;
-        const int32_t mv = (int32_t)seg_size(S, jj + 1, 2 * uv + 1);
+        if (uv >= S.N) continue;
+        // ss(uv) and ss(lChild(uv)) from the level's constants (32-bit: uv < 2^31)
+        const int32_t B = a.lv[jj].B, half = B >> 1;
+        const int32_t rm = M - ((int32_t)uv - ((1 << jj) - 1)) * B;
+        const int32_t nv = B - 1 + (rm < 0 ? 0 : (rm > B ? B : rm));
+        const int32_t mv = jj + 1 < S.L ? half - 1 + (rm < 0 ? 0 : (rm > half ? half : rm)) : 0;
         const int32_t iv = (irel << lev) + vl;
-        const int d = a.mode == KDT_SPLIT_ROUND_ROBIN ? jj % k : sf_widest_dim(a, sm, s0, jj - a.l0, iv);
+        int d;
+        if (a.mode == KDT_SPLIT_ROUND_ROBIN) {
+            d = d0 + lev;
+            while (d >= k) d -= k;
+        } else {
+            d = sf_widest_dim(a, sm, s0, jj - a.l0, iv);
+        }
         const bool leaves = nv <= 3;
         if (leaves && v < 7) done |= 3u << (2 * v + 1);
         const uint16_t *seg = A + d * T + o;
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
     const int64_t s0 = full_nodes(a.l0) + blockIdx.x;
     const uint32_t n = (uint32_t)seg_size(S, a.l0, s0);
     const int64_t base = seg_begin(S, a.l0, s0);
-    if (n > (uint32_t)T || (uint32_t)T > kSfPPT * NT || (uint32_t)nb % NT != 0u || nb > 65536) {
+    if (n > (uint32_t)T || (uint32_t)T > kSfPPT * NT || (uint32_t)nb % (2u * NT) != 0u || nb > 65536) {
         if (tid == 0) {
             set_status(a.status, KDT_EINTERNAL);
             a.fallback[blockIdx.x] = 0;
@@ -400,7 +411,7 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
             fail = true;
             break;
         }
-        for (uint32_t b = tid; b < (uint32_t)nb; b += NT) sm.hist[b] = 0u;
+        for (uint32_t b = tid; b < (uint32_t)nb / 2u; b += NT) sm.hist[b] = 0u;
         __syncthreads();
         uint32_t pk[kSfPPT];
 #pragma unroll
@@ -409,15 +420,17 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
             pk[i] = 0u;
             if (q < n) {
                 const uint32_t b = spread ? value_bucket(kc[q], lo, scale, (uint32_t)nb) : 0u;
-                pk[i] = (b << 16) | atomicAdd(&sm.hist[b], 1u);
+                const uint32_t sh = (b & 1u) << 4;
+                pk[i] = (b << 16) | ((atomicAdd(&sm.hist[b >> 1], 1u << sh) >> sh) & 0xffffu);
             }
         }
         __syncthreads();
         const uint32_t per = (uint32_t)nb / NT;
+        uint16_t *h16 = reinterpret_cast<uint16_t *>(sm.hist);  // counters, then bucket starts
         uint32_t sum = 0u;
         int big = 0;
         for (uint32_t i = 0; i < per; ++i) {
-            const uint32_t h = sm.hist[tid * per + i];
+            const uint32_t h = h16[tid * per + i];
             sum += h;
             big |= h > (uint32_t)kSfMaxBucket;
         }
@@ -427,15 +440,15 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
         }
         uint32_t run = block_exclusive_scan(sum, red);
         for (uint32_t i = 0; i < per; ++i) {
-            const uint32_t h = sm.hist[tid * per + i];
-            sm.hist[tid * per + i] = run;
+            const uint32_t h = h16[tid * per + i];
+            h16[tid * per + i] = (uint16_t)run;
             run += h;
         }
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < kSfPPT; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
-            if (q < n) sm.stage[sm.hist[pk[i] >> 16] + (pk[i] & 0xffffu)] = (uint16_t)q;
+            if (q < n) sm.stage[h16[pk[i] >> 16] + (pk[i] & 0xffffu)] = (uint16_t)q;
         }
         __syncthreads();
         // rank inside the bucket under the super key of c
@@ -445,7 +458,7 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
             const uint32_t q = tid + (uint32_t)i * NT;
             if (q < n) {
                 const uint32_t b = pk[i] >> 16;
-                const uint32_t beg = sm.hist[b], end = b + 1 < (uint32_t)nb ? sm.hist[b + 1] : n;
+                const uint32_t beg = h16[b], end = b + 1 < (uint32_t)nb ? h16[b + 1] : n;
                 uint32_t rank = 0u;
                 if (end - beg > 1u) {
                     const uint32_t kq = kc[q];
@@ -583,7 +596,7 @@ int pick_tile(int k, int mode, TilePlan *tp) {
     static const int cands[] = {4096, 2048, 1024, 512};
     for (int T : cands) {
         if (T > kSfPPT * kSfThreads) continue;
-        const int nb = T / 2 > kSfThreads ? T / 2 : kSfThreads;
+        const int nb = T > 2 * kSfThreads ? T : 2 * kSfThreads;  // about one point per bucket
         const size_t a = sorted_finisher_smem(k, T, mode, nb);
         const size_t b = select_finisher_smem(k, T, mode);
         if (a <= kSfSmemBudget && b <= kSelectSmemMax) {
