@@ -67,6 +67,6 @@ def test_recorded_traffic_tracks_kernel_source(tmp_path, monkeypatch):
     shutil.copy(os.path.join(bench.ROOT, "profiles", "traffic_uniform_100m.txt"), root / "profiles")
     src = root / "balanced_tree_build_gb300" / "csrc"
     src.mkdir(parents=True)
-    (src / "kdt_finisher.cu").write_text("// changed\n")
+    (src / "kdt_finisher_sorted.cu").write_text("// changed\n")
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.recorded_traffic("finisher") is None
