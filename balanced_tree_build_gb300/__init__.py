@@ -63,13 +63,16 @@ def _load():
     L.kdt_build_ws.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
     L.kdt_build_host.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
     L.kdt_verify.argtypes = [vp, i64, i32, i32, vp, vp]
+    L.kdt_gather_points.argtypes = [vp, i64, i32, vp, vp, vp]
+    L.kdt_build_inplace.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
     L.kdt_status.argtypes = [vp]
     L.kdt_error_string.argtypes = [i32]
     L.kdt_error_string.restype = ctypes.c_char_p
     L.kdt_profile_enable.argtypes = [i32]
     L.kdt_profile_read.argtypes = [ctypes.POINTER(_KernelStat), i32]
     for name in ("kdt_workspace_size", "kdt_host_workspace_size", "kdt_build", "kdt_build_ws",
-                 "kdt_build_host", "kdt_verify", "kdt_status", "kdt_profile_enable",
+                 "kdt_build_host", "kdt_verify", "kdt_gather_points", "kdt_build_inplace", "kdt_status",
+                 "kdt_profile_enable",
                  "kdt_profile_reset", "kdt_profile_read"):
         getattr(L, name).restype = i32
     _lib = L
@@ -202,6 +205,44 @@ def verify_tree(points, perm, mode: int = SPLIT_ROUND_ROBIN, stream=None) -> boo
                             ctypes.c_void_p(perm.data_ptr()), _stream_ptr(stream))
     _check(rc, "kdt_verify")
     return rc == 0
+
+
+def gather_points(points, perm, out=None, stream=None):
+    """The points in level order: out[node] = points[perm[node]] (CUDA float32
+    [N, k], bit-exact).  ``out`` must not overlap ``points``.  Stream-ordered;
+    a bad ``perm`` entry shows up in status()."""
+    import torch
+    n, k = _check_points(points)
+    if perm.dtype != torch.int32 or perm.shape != (n,) or not perm.is_cuda or not perm.is_contiguous():
+        raise ValueError("perm must be a contiguous CUDA int32 tensor of shape (N,)")
+    if out is None:
+        out = torch.empty_like(points)
+    elif out.dtype != torch.float32 or out.shape != points.shape or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA float32 tensor shaped like points")
+    rc = _load().kdt_gather_points(ctypes.c_void_p(points.data_ptr()), n, k, ctypes.c_void_p(perm.data_ptr()),
+                                   ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    _check(rc, "kdt_gather_points")
+    return out
+
+
+def build_inplace(points, mode: int = SPLIT_ROUND_ROBIN, perm=None, workspace=None, stream=None):
+    """Builds the tree of ``points`` (CUDA float32 [N, k]) and rewrites
+    ``points`` in level order (row node = the point stored at node); returns
+    the int32 permutation.  ``workspace`` (from alloc_workspace) is the only
+    temporary; one is allocated if omitted.  Stream-ordered."""
+    import torch
+    n, k = _check_points(points)
+    if perm is None:
+        perm = torch.empty(n, dtype=torch.int32, device=points.device)
+    elif perm.dtype != torch.int32 or perm.shape != (n,) or not perm.is_cuda or not perm.is_contiguous():
+        raise ValueError("perm must be a contiguous CUDA int32 tensor of shape (N,)")
+    if workspace is None:
+        workspace = alloc_workspace(n, k, mode, device=points.device)
+    rc = _load().kdt_build_inplace(ctypes.c_void_p(points.data_ptr()), n, k, mode, ctypes.c_void_p(perm.data_ptr()),
+                                   ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(rc, "kdt_build_inplace")
+    return perm
 
 
 def status(stream=None) -> int:

@@ -20,6 +20,12 @@ __global__ void status_fold_kernel(const int *s) {
 
 void enqueue_status_fold(int *status, cudaStream_t stream) { status_fold_kernel<<<1, 1, 0, stream>>>(status); }
 
+int *device_status_address() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    return static_cast<int *>(p);
+}
+
 int read_and_clear_device_status(int *out) {
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return KDT_ECUDA;
@@ -185,6 +191,31 @@ int kdt_verify(const float *pts, int64_t N, int k, int split_mode, const int32_t
     const int rc = enqueue_verify(pts, N, k, split_mode, perm, static_cast<cudaStream_t>(stream), &result);
     if (rc != KDT_OK) return rc;
     return result;
+}
+
+int kdt_gather_points(const float *pts, int64_t N, int k, const int32_t *perm, float *out, void *stream) {
+    if (!pts || !perm || !out || N < 1 || N > 2147483647LL || k < 1 || k > kMaxK) return KDT_EINVAL;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(pts), a1 = a0 + (uintptr_t)N * k * 4;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(out), b1 = b0 + (uintptr_t)N * k * 4;
+    if (a0 < b1 && b0 < a1) return KDT_EINVAL;  // out overlaps pts
+    int *st = device_status_address();
+    if (!st) return KDT_ECUDA;
+    return enqueue_gather(pts, N, k, perm, out, st, static_cast<cudaStream_t>(stream));
+}
+
+int kdt_build_inplace(float *pts, int64_t N, int k, int split_mode, int32_t *perm, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (!pts || !perm || !workspace) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, split_mode, &p);
+    if (rc != KDT_OK) return rc;
+    if (workspace_bytes < p.bytes) return KDT_ENOMEM;
+    if (!aligned256(workspace)) return KDT_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Buffers b = carve(p, workspace);
+    const int rb = enqueue_build(p, b, pts, perm, s);
+    if (rb != KDT_OK) return rb;
+    return enqueue_inplace_tail(p, b, pts, perm, s);
 }
 
 int kdt_status(void *stream) {

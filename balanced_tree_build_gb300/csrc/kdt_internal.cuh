@@ -224,4 +224,14 @@ int read_and_clear_device_status(int *out);
 int enqueue_verify(const float *pts, int64_t N, int k, int mode, const int32_t *perm,
                    cudaStream_t stream, int *result);
 
+// Level-order points (kdt_gather.cu): out[u] = pts[perm[u]] (rows of k
+// words); bad perm entries are recorded in *status.
+int enqueue_gather(const float *pts, int64_t N, int k, const int32_t *perm, float *out, int *status,
+                   cudaStream_t stream);
+// After enqueue_build: rewrites pts in level order through the workspace
+// (skipped if the build recorded an error).
+int enqueue_inplace_tail(const Plan &p, const Buffers &b, float *pts, const int32_t *perm, cudaStream_t stream);
+// Device address of the calling thread's current device's status word.
+int *device_status_address();
+
 }  // namespace kdt

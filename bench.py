@@ -258,6 +258,49 @@ def workload_config(w, extra=None) -> dict:
 # ---------------------------------------------------------------------------
 # our build
 
+def level_order_extra(kdt, pts, perm, ws, workload, stream, peak) -> dict:
+    """Times the points-in-level-order gather (kdt_gather_points) on the bench
+    workload's tree, and the in-place build (kdt_build_inplace) on a copy of
+    the points; checks a sample of the gathered rows bit for bit."""
+    import torch
+    n, k = pts.shape
+    out = torch.empty_like(pts)
+    for _ in range(2):
+        kdt.gather_points(pts, perm, out=out, stream=stream)
+    reps = 5
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        kdt.gather_points(pts, perm, out=out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    gather_ms = e0.elapsed_time(e1) / reps
+    if kdt.status(stream) != 0:
+        raise SystemExit("device status after the gather")
+    idx = torch.randint(0, n, (min(n, 1 << 20),), device=pts.device)
+    if not torch.equal(out[idx].view(torch.int32), pts[perm[idx].long()].view(torch.int32)):
+        raise SystemExit("gathered rows differ from pts[perm]")
+    alg = float(n) * (4 + 8 * k)  # perm read, row read, row write
+    scratch = torch.empty_like(pts)
+    times = []
+    for i in range(3):
+        scratch.copy_(pts)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kdt.build_inplace(scratch, workload.mode, perm=perm, workspace=ws, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            times.append(a.elapsed_time(b))
+    if kdt.status(stream) != 0:
+        raise SystemExit("device status after the in-place build")
+    return {"gather_ms": gather_ms, "gather_alg_bytes": alg, "gather_GBps": alg / (gather_ms / 1e3) / 1e9,
+            "gather_frac_of_measured": alg / (gather_ms / 1e3) / 1e9 / peak,
+            "inplace_build_ms": sum(times) / len(times), "api": "kdt_gather_points, kdt_build_inplace"}
+
+
 def run_ours(args, workload):
     import torch
     import balanced_tree_build_gb300 as kdt
@@ -347,6 +390,10 @@ def run_ours(args, workload):
                "steps": e_steps, "api": "kdt_build_host (pinned host buffers)"}
         del hws
 
+    extras = None
+    if not args.no_extras:
+        extras = {"level_order_points": level_order_extra(kdt, pts, perm, ws, workload, stream, peak)}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(workload)
@@ -358,7 +405,7 @@ def run_ours(args, workload):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(workload, extra={"parallelism": f"replicas x{world}"}),
             "roofline": roofline, "build_roofline": build_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "kernels": stats, "clocks": clocks,
+            "gpu_launches": launches, "kernels": stats, "clocks": clocks, "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if active:
@@ -376,6 +423,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="uniform_100m")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the level-order points timing")
     ap.add_argument("--ref-sample", type=int, default=1 << 18,
                     help="points per step for --impl reference")
     ap.add_argument("--n", type=int, default=None,

@@ -111,6 +111,30 @@ int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode,
 int kdt_verify(const float *pts, int64_t N, int k, int split_mode,
                const int32_t *perm, void *stream);
 
+/* The points in level order: out[node * k + c] = pts[perm[node] * k + c] for
+ * every node and coordinate, copied as raw 32-bit words (bit-exact, signed
+ * zeros included).  This applies a build's permutation to the data, the
+ * reordered point array that "GPU-friendly, Parallel, and (Almost-)In-Place
+ * Construction of Left-Balanced k-d Trees" produces (introduction, core
+ * idea).  pts (N x k, read-only), perm (int32[N], read-only) and out (N x k,
+ * fully overwritten) are DEVICE pointers owned by the caller; out must not
+ * overlap pts (KDT_EINVAL).  An entry of perm outside 0..N-1 is skipped and
+ * recorded as KDT_EINVAL in the device status word (kdt_status).
+ * Allocates nothing.  Stream-ordered. */
+int kdt_gather_points(const float *pts, int64_t N, int k, const int32_t *perm,
+                      float *out, void *stream);
+
+/* In-place build: builds the tree of pts exactly as kdt_build_ws (perm
+ * receives the permutation), then rewrites pts itself in level order, so that
+ * afterwards pts[node * k + c] is coordinate c of the point stored at `node`
+ * (bit-exact).  `workspace` (at least kdt_workspace_size() bytes, 256-byte
+ * aligned) is the only temporary; nothing is allocated.  pts is read by the
+ * build before it is rewritten; if the build records a device-side error, pts
+ * is left unchanged.  pts and perm are DEVICE pointers.  Stream-ordered. */
+int kdt_build_inplace(float *pts, int64_t N, int k, int split_mode,
+                      int32_t *perm, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
 /* Synchronises `stream`, then returns and clears the calling thread's current
  * device's status word (KDT_OK if no device-side error was recorded). */
 int kdt_status(void *stream);

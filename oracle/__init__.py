@@ -2,8 +2,10 @@
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference leg may import this package.  The CUDA library never imports it and
-shares no code with it.  Every function here is a thin ctypes wrapper around
-``kdt_oracle.c``; see that file's header for the passages each routine follows.
+shares no code with it.  Every tree routine here is a thin ctypes wrapper
+around ``kdt_oracle.c``; see that file's header for the passages each routine
+follows.  ``gather_points`` (the points in level order) is its definition
+written out with numpy indexing.
 """
 from __future__ import annotations
 
@@ -159,3 +161,21 @@ def get() -> Oracle:
     if _default is None:
         _default = Oracle(0)
     return _default
+
+
+def gather_points(pts: np.ndarray, perm: np.ndarray) -> np.ndarray:
+    """The points in level order: row ``node`` of the result is row
+    ``perm[node]`` of ``pts``, copied as raw 32-bit words (signed zeros kept).
+    "GPU-friendly, Parallel, and (Almost-)In-Place Construction of
+    Left-Balanced k-d Trees" (introduction, core idea): the build leaves the
+    data array itself in the tree's order.  ``perm`` must be a permutation of
+    0..N-1."""
+    pts = _points(pts)
+    perm = np.asarray(perm)
+    n = pts.shape[0]
+    if perm.shape != (n,) or not np.issubdtype(perm.dtype, np.integer):
+        raise ValueError("perm must be an integer array of shape (N,)")
+    if n and (perm.min() < 0 or perm.max() >= n or np.unique(perm).size != n):
+        raise ValueError("perm must be a permutation of 0..N-1")
+    words = pts.view(np.uint32)
+    return np.ascontiguousarray(words[perm.astype(np.int64)]).view(np.float32)
