@@ -65,13 +65,16 @@ def _load():
     L.kdt_verify.argtypes = [vp, i64, i32, i32, vp, vp]
     L.kdt_gather_points.argtypes = [vp, i64, i32, vp, vp, vp]
     L.kdt_build_inplace.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
+    L.kdt_node_dims.argtypes = [vp, i64, i32, i32, vp, vp]
+    L.kdt_knn.argtypes = [vp, i64, i32, vp, vp, i64, i32, vp, vp, vp]
     L.kdt_status.argtypes = [vp]
     L.kdt_error_string.argtypes = [i32]
     L.kdt_error_string.restype = ctypes.c_char_p
     L.kdt_profile_enable.argtypes = [i32]
     L.kdt_profile_read.argtypes = [ctypes.POINTER(_KernelStat), i32]
     for name in ("kdt_workspace_size", "kdt_host_workspace_size", "kdt_build", "kdt_build_ws",
-                 "kdt_build_host", "kdt_verify", "kdt_gather_points", "kdt_build_inplace", "kdt_status",
+                 "kdt_build_host", "kdt_verify", "kdt_gather_points", "kdt_build_inplace", "kdt_node_dims",
+                 "kdt_knn", "kdt_status",
                  "kdt_profile_enable",
                  "kdt_profile_reset", "kdt_profile_read"):
         getattr(L, name).restype = i32
@@ -243,6 +246,45 @@ def build_inplace(points, mode: int = SPLIT_ROUND_ROBIN, perm=None, workspace=No
                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(rc, "kdt_build_inplace")
     return perm
+
+
+def node_dims(tree_points, mode: int = SPLIT_ROUND_ROBIN, out=None, stream=None):
+    """Split dimension of every node (CUDA uint8 [N]) of the tree whose points
+    in level order are ``tree_points``.  Stream-ordered."""
+    import torch
+    n, k = _check_points(tree_points)
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=tree_points.device)
+    elif out.dtype != torch.uint8 or out.shape != (n,) or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA uint8 tensor of shape (N,)")
+    rc = _load().kdt_node_dims(ctypes.c_void_p(tree_points.data_ptr()), n, k, mode,
+                               ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    _check(rc, "kdt_node_dims")
+    return out
+
+
+def knn(tree_points, queries, K: int, dims=None, out_nodes=None, out_dist2=None, stream=None):
+    """The K nearest nodes of each query: (int32 [Q, K] node ids, float32
+    [Q, K] squared distances), ascending by (dist2, node).  ``dims``: the
+    tree's split dimensions (node_dims); None means round-robin.
+    Stream-ordered."""
+    import torch
+    n, k = _check_points(tree_points)
+    qn, qk = _check_points(queries)
+    if qk != k:
+        raise ValueError("queries must have the tree's k columns")
+    if out_nodes is None:
+        out_nodes = torch.empty((qn, K), dtype=torch.int32, device=queries.device)
+    if out_dist2 is None:
+        out_dist2 = torch.empty((qn, K), dtype=torch.float32, device=queries.device)
+    if dims is not None and (dims.dtype != torch.uint8 or dims.shape != (n,) or not dims.is_cuda):
+        raise ValueError("dims must be a CUDA uint8 tensor of shape (N,)")
+    rc = _load().kdt_knn(ctypes.c_void_p(tree_points.data_ptr()), n, k,
+                         ctypes.c_void_p(dims.data_ptr()) if dims is not None else None,
+                         ctypes.c_void_p(queries.data_ptr()), qn, K, ctypes.c_void_p(out_nodes.data_ptr()),
+                         ctypes.c_void_p(out_dist2.data_ptr()), _stream_ptr(stream))
+    _check(rc, "kdt_knn")
+    return out_nodes, out_dist2
 
 
 def status(stream=None) -> int:

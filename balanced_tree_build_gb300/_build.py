@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libkdtree_gb300.so")
-SOURCES = ["kdt_build.cu", "kdt_levels.cu", "kdt_finisher.cu", "kdt_finisher_sorted.cu", "kdt_verify.cu", "kdt_api.cu", "kdt_static.cu", "kdt_gather.cu"]
+SOURCES = ["kdt_build.cu", "kdt_levels.cu", "kdt_finisher.cu", "kdt_finisher_sorted.cu", "kdt_verify.cu", "kdt_api.cu", "kdt_static.cu", "kdt_gather.cu", "kdt_query.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -218,6 +218,24 @@ int kdt_build_inplace(float *pts, int64_t N, int k, int split_mode, int32_t *per
     return enqueue_inplace_tail(p, b, pts, perm, s);
 }
 
+int kdt_node_dims(const float *tree_pts, int64_t N, int k, int split_mode, uint8_t *dims, void *stream) {
+    if (!tree_pts || !dims || N < 1 || N > 2147483647LL || k < 1 || k > kMaxK ||
+        (split_mode != KDT_SPLIT_ROUND_ROBIN && split_mode != KDT_SPLIT_WIDEST))
+        return KDT_EINVAL;
+    return enqueue_node_dims(tree_pts, N, k, split_mode, dims, static_cast<cudaStream_t>(stream));
+}
+
+int kdt_knn(const float *tree_pts, int64_t N, int k, const uint8_t *dims, const float *queries, int64_t Q, int K,
+            int32_t *out_node, float *out_dist2, void *stream) {
+    if (!tree_pts || !queries || !out_node || !out_dist2 || N < 1 || N > 2147483647LL || k < 1 || k > kMaxK ||
+        Q < 0 || K < 1 || K > KDT_MAX_KNN)
+        return KDT_EINVAL;
+    int *st = device_status_address();
+    if (!st) return KDT_ECUDA;
+    return enqueue_knn(tree_pts, N, k, dims, queries, Q, K, out_node, out_dist2, st,
+                       static_cast<cudaStream_t>(stream));
+}
+
 int kdt_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDT_ECUDA;
     int v = 0;

@@ -234,4 +234,9 @@ int enqueue_inplace_tail(const Plan &p, const Buffers &b, float *pts, const int3
 // Device address of the calling thread's current device's status word.
 int *device_status_address();
 
+// Queries on a built tree (kdt_query.cu).
+int enqueue_node_dims(const float *tree_pts, int64_t N, int k, int mode, uint8_t *dims, cudaStream_t stream);
+int enqueue_knn(const float *tree_pts, int64_t N, int k, const uint8_t *dims, const float *queries, int64_t Q,
+                int K, int32_t *out_node, float *out_dist2, int *status, cudaStream_t stream);
+
 }  // namespace kdt

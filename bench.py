@@ -296,9 +296,36 @@ def level_order_extra(kdt, pts, perm, ws, workload, stream, peak) -> dict:
             times.append(a.elapsed_time(b))
     if kdt.status(stream) != 0:
         raise SystemExit("device status after the in-place build")
-    return {"gather_ms": gather_ms, "gather_alg_bytes": alg, "gather_GBps": alg / (gather_ms / 1e3) / 1e9,
-            "gather_frac_of_measured": alg / (gather_ms / 1e3) / 1e9 / peak,
-            "inplace_build_ms": sum(times) / len(times), "api": "kdt_gather_points, kdt_build_inplace"}
+    res = {"gather_ms": gather_ms, "gather_alg_bytes": alg, "gather_GBps": alg / (gather_ms / 1e3) / 1e9,
+           "gather_frac_of_measured": alg / (gather_ms / 1e3) / 1e9 / peak,
+           "inplace_build_ms": sum(times) / len(times), "api": "kdt_gather_points, kdt_build_inplace"}
+    return res, out
+
+
+def knn_extra(kdt, tree_pts, workload, stream, n_queries: int = 1 << 20, K: int = 8) -> dict:
+    """Times kdt_knn: n_queries points drawn from the workload's distribution
+    (another seed) against the tree whose level-order points are tree_pts."""
+    import torch
+    from balanced_tree_build_gb300.inputs import make_points
+    n, k = tree_pts.shape
+    q = torch.from_numpy(make_points(workload.dist, n_queries, k, workload.seed + 1000)).to(tree_pts.device)
+    dims = kdt.node_dims(tree_pts, workload.mode, stream=stream) if workload.mode == 1 else None
+    nodes = torch.empty((n_queries, K), dtype=torch.int32, device=q.device)
+    d2 = torch.empty((n_queries, K), dtype=torch.float32, device=q.device)
+    kdt.knn(tree_pts, q, K, dims=dims, out_nodes=nodes, out_dist2=d2, stream=stream)
+    reps = 3
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        kdt.knn(tree_pts, q, K, dims=dims, out_nodes=nodes, out_dist2=d2, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if kdt.status(stream) != 0:
+        raise SystemExit("device status after kNN queries")
+    ms = e0.elapsed_time(e1) / reps
+    return {"queries": n_queries, "K": K, "ms": ms, "queries_per_s": n_queries / (ms / 1e3),
+            "tree_points": n, "api": "kdt_knn (one thread per query, stack-free descent and backtrack)"}
 
 
 def run_ours(args, workload):
@@ -392,7 +419,9 @@ def run_ours(args, workload):
 
     extras = None
     if not args.no_extras:
-        extras = {"level_order_points": level_order_extra(kdt, pts, perm, ws, workload, stream, peak)}
+        lo, tree_pts = level_order_extra(kdt, pts, perm, ws, workload, stream, peak)
+        extras = {"level_order_points": lo, "knn": knn_extra(kdt, tree_pts, workload, stream)}
+        del tree_pts
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -135,6 +135,43 @@ int kdt_build_inplace(float *pts, int64_t N, int k, int split_mode,
                       int32_t *perm, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* ---- queries on a built tree ------------------------------------------------
+ * tree_pts is the tree's points in level order (row u = the point stored at
+ * node u: the output of kdt_gather_points or kdt_build_inplace), N x k float32,
+ * a DEVICE pointer.  Results refer to node ids; perm[node] gives the input
+ * index. */
+
+/* Split dimension of every node: dims[u] (uint8[N], DEVICE, fully
+ * overwritten).  Round-robin: level(u) mod k.  Widest: the walk of the
+ * split-widest-dimension paragraphs of the left-balanced paper -- the root's
+ * domain is the bounding box of all points, each step down cuts it at the
+ * ancestor's split coordinate, the node's dimension is the widest extent of
+ * its domain (float32 hi - lo, lowest dimension on ties) -- which are the
+ * dimensions the build used.  Allocates 2k words stream-ordered (widest).
+ * Stream-ordered. */
+int kdt_node_dims(const float *tree_pts, int64_t N, int k, int split_mode,
+                  uint8_t *dims, void *stream);
+
+#define KDT_MAX_KNN 64
+
+/* The K nearest nodes of each query ("Bigger Buffer k-d Trees on
+ * Multi-Many-Core Systems", nearest-neighbour search via k-d trees: down to
+ * the query's cell, then back up, entering a node's other subtree only when
+ * its splitting plane is within the current K-th distance; no stack on the
+ * implicit tree).  Result: for query i, out_node[i*K + j] and
+ * out_dist2[i*K + j] (j = 0..K-1) are the K smallest pairs (dist2, node) in
+ * lexicographic order, ascending, where dist2 = sum over c = 0..k-1 of
+ * (q[c] - p[c])^2 accumulated left to right in float32 with every operation
+ * rounded (no fused multiply-add).  Slots beyond N hold node -1 and dist2
+ * +infinity.  dims: the tree's split dimensions (kdt_node_dims); NULL means
+ * round-robin.  queries is Q x k float32; all pointers are DEVICE pointers,
+ * out_* fully overwritten.  1 <= K <= KDT_MAX_KNN, Q >= 0.  A dims entry >= k
+ * is recorded as KDT_EINVAL in the device status word.  Allocates nothing.
+ * Stream-ordered. */
+int kdt_knn(const float *tree_pts, int64_t N, int k, const uint8_t *dims,
+            const float *queries, int64_t Q, int K, int32_t *out_node,
+            float *out_dist2, void *stream);
+
 /* Synchronises `stream`, then returns and clears the calling thread's current
  * device's status word (KDT_OK if no device-side error was recorded). */
 int kdt_status(void *stream);

@@ -76,6 +76,12 @@ class Oracle:
         L.kdo_verify.restype = i32
         L.kdo_brute_force.argtypes = [f32p, i32, i32, i32, f32p]
         L.kdo_brute_force.restype = i64
+        L.kdo_node_dims.argtypes = [f32p, i64, i32, i32, f32p]
+        L.kdo_node_dims.restype = i32
+        L.kdo_dist2.argtypes = [f32p, f32p, i32]
+        L.kdo_dist2.restype = ctypes.c_float
+        L.kdo_knn_brute.argtypes = [f32p, i64, i32, f32p, i64, i32, f32p, f32p]
+        L.kdo_knn_brute.restype = i32
 
     # -- notation ---------------------------------------------------------
     def level(self, i: int) -> int:
@@ -127,6 +133,38 @@ class Oracle:
         if rc < 0:
             raise OracleError(rc)
         return rc == 0, int(bad.value)
+
+    # -- queries on a built tree (tree_pts = the points in level order) -------
+    def node_dims(self, tree_pts: np.ndarray, mode: int = 0) -> np.ndarray:
+        """Split dimension of every node (uint8[N])."""
+        tree_pts = _points(tree_pts)
+        n, k = tree_pts.shape
+        dims = np.empty(n, dtype=np.uint8)
+        rc = self.lib.kdo_node_dims(tree_pts.ctypes.data, n, k, mode, dims.ctypes.data)
+        if rc != OK:
+            raise OracleError(rc)
+        return dims
+
+    def dist2(self, q: np.ndarray, p: np.ndarray) -> float:
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        p = np.ascontiguousarray(p, dtype=np.float32)
+        return float(self.lib.kdo_dist2(q.ctypes.data, p.ctypes.data, q.size))
+
+    def knn(self, tree_pts: np.ndarray, queries: np.ndarray, K: int):
+        """Brute-force K nearest nodes: (node int32[Q, K], dist2 float32[Q, K])."""
+        tree_pts = _points(tree_pts)
+        queries = _points(queries)
+        n, k = tree_pts.shape
+        if queries.shape[1] != k:
+            raise ValueError("queries must have k columns")
+        qn = queries.shape[0]
+        nodes = np.empty((qn, K), dtype=np.int32)
+        d2 = np.empty((qn, K), dtype=np.float32)
+        rc = self.lib.kdo_knn_brute(tree_pts.ctypes.data, n, k, queries.ctypes.data, qn, K,
+                                    nodes.ctypes.data, d2.ctypes.data)
+        if rc != OK:
+            raise OracleError(rc)
+        return nodes, d2
 
     def brute_force(self, pts: np.ndarray, mode: int = 0):
         """Returns (number of valid orderings, first valid ordering)."""

@@ -411,3 +411,102 @@ int64_t kdo_brute_force(const float *pts, int N, int k, int mode,
     }
     return valid;
 }
+
+/* ---- split dimensions of a built tree -------------------------------------
+ * dims[u] = the split dimension of level-order node u of the tree whose points
+ * in level order are tree_pts (row u = the point stored at node u).
+ * Round-robin ([W] round-robin paragraph): level(u) mod k.  Widest ([W]
+ * split-widest-dimension paragraphs, the walk): start from the bounding box of
+ * all points, go down from the root to u, cutting the domain at each
+ * ancestor's split coordinate (hi for a left turn, lo for a right turn), and
+ * take the widest extent of the final domain. */
+int kdo_node_dims(const float *tree_pts, int64_t N, int k, int mode, uint8_t *dims)
+{
+    int rc = check_args(tree_pts, N, k, mode);
+    if (rc != KDO_OK || !dims)
+        return rc != KDO_OK ? rc : KDO_EINVAL;
+    float root_lo[KDO_MAXK], root_hi[KDO_MAXK];
+    bbox(tree_pts, N, k, root_lo, root_hi);
+    for (int64_t u = 0; u < N; u++) {
+        int depth = kdo_level(u);
+        if (mode == 0) {
+            dims[u] = (uint8_t)(depth % k);
+            continue;
+        }
+        float lo[KDO_MAXK], hi[KDO_MAXK];
+        memcpy(lo, root_lo, sizeof(float) * k);
+        memcpy(hi, root_hi, sizeof(float) * k);
+        int64_t a = 0; /* current ancestor */
+        for (int t = depth - 1; t >= 0; t--) {
+            int d = kdo_widest_dim(lo, hi, k);
+            int right = (int)(((u + 1) >> t) & 1);
+            float s = tree_pts[a * k + d];
+            if (right)
+                lo[d] = s;
+            else
+                hi[d] = s;
+            a = 2 * a + 1 + right;
+        }
+        if (a != u)
+            return KDO_EINTERNAL;
+        dims[u] = (uint8_t)kdo_widest_dim(lo, hi, k);
+    }
+    return KDO_OK;
+}
+
+/* ---- k nearest neighbours, by brute force ----------------------------------
+ * "Bigger Buffer k-d Trees on Multi-Many-Core Systems", nearest-neighbour
+ * problem statement: the K points of the reference set closest to a query in
+ * Euclidean distance.  Readings (listed in the design doc): the distance is the
+ * squared distance sum_{c=0..k-1} (q[c] - p[c])^2, accumulated left to right
+ * in float32 with every operation rounded (no fused multiply-add); the
+ * reference points are the tree's nodes; the result is the K smallest pairs
+ * (distance, node id) in that lexicographic order, listed ascending -- unique
+ * because node ids are distinct.  When N < K the remaining slots hold node -1
+ * and distance +infinity. */
+float kdo_dist2(const float *q, const float *p, int k)
+{
+    float d = 0.0f;
+    for (int c = 0; c < k; c++) {
+        float t = q[c] - p[c];
+        d = d + t * t;
+    }
+    return d;
+}
+
+int kdo_knn_brute(const float *tree_pts, int64_t N, int k, const float *queries, int64_t Q, int K,
+                  int32_t *out_node, float *out_dist2)
+{
+    if (!tree_pts || !queries || !out_node || !out_dist2 || N < 1 || N > INT32_MAX || k < 1 ||
+        k > KDO_MAXK || Q < 0 || K < 1)
+        return KDO_EINVAL;
+    for (int64_t qi = 0; qi < Q; qi++) {
+        const float *q = queries + qi * k;
+        int32_t *bn = out_node + qi * K;
+        float *bd = out_dist2 + qi * K;
+        int have = 0; /* bn/bd[0..have) sorted ascending by (distance, node) */
+        for (int64_t u = 0; u < N; u++) {
+            float d = kdo_dist2(q, tree_pts + u * k, k);
+            if (have == K) {
+                /* not better than the worst kept pair: skip */
+                if (!(d < bd[K - 1] || (d == bd[K - 1] && u < bn[K - 1])))
+                    continue;
+                have--;
+            }
+            int j = have;
+            while (j > 0 && (d < bd[j - 1] || (d == bd[j - 1] && u < bn[j - 1]))) {
+                bd[j] = bd[j - 1];
+                bn[j] = bn[j - 1];
+                j--;
+            }
+            bd[j] = d;
+            bn[j] = (int32_t)u;
+            have++;
+        }
+        for (int j = have; j < K; j++) {
+            bn[j] = -1;
+            bd[j] = INFINITY;
+        }
+    }
+    return KDO_OK;
+}
