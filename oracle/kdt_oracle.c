@@ -22,6 +22,9 @@
  *        (Robinson, KdTreeGPU wiki), sort paragraph: on equal primary
  *        coordinates compare the next coordinate, then the next, ... (the
  *        "super key").
+ *   [B]  "Bigger Buffer k-d Trees on Multi-Many-Core Systems", nearest
+ *        neighbour problem statement (K nearest reference points of a query
+ *        in Euclidean distance) -- for the query routines at the end.
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - the super key is cyclic from the split dimension p: (x[p], x[p+1 mod k],
