@@ -521,18 +521,38 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
     }
 
     // 4. lower levels: warp w owns nodes [w*cnt/W, (w+1)*cnt/W) of every
-    //    level and splits them node by node.  Its subtrees stay packed from
-    //    the offset `wbase` where it took them over: in the tile-wide layout a
-    //    warp's range moves left level by level (split points leave) and
-    //    would reach ranges that a slower neighbour still reads.
+    //    level.  Its subtrees stay packed from the offset `wbase` where it
+    //    took them over: in the tile-wide layout a warp's range moves left
+    //    level by level (split points leave) and would reach ranges that a
+    //    slower neighbour still reads.  A warp owns at most 8 nodes per level
+    //    here (this phase starts with one node per warp and ends at level L-5
+    //    of tiles of at most 4096 points), so lane l holds the constants of
+    //    its l-th node -- start of its segment, ss(lChild), left points of the
+    //    nodes before it, split dimension -- and every position finds them by
+    //    one shuffle from the byte that names its node (written when the
+    //    point moved to its child on the level above).  Each array is then
+    //    split in one pass over the warp's range, with no per-node loops: the
+    //    array of a node's split dimension by offset, the others by side flag
+    //    and running left/right counts (left point: Lpre + right points of
+    //    the earlier nodes; right point: Rpre + their left points + m).
     bool warp_owned = false;
     int32_t wbase = 0;
     if (j + 4 < S.L) {
         warp_owned = true;
+        uint8_t *pcur = reinterpret_cast<uint8_t *>(sm.stage), *pnxt = pcur + T;  // warp-local node of each position
         {
             const int depth = j - a.l0;
             const int64_t first = ((s0 + 1) << depth) - 1;
-            wbase = make_tile_level(S, a.lv[j], j, first).off((int32_t)w * ((1 << depth) / kSfWarps));
+            const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
+            const int32_t per = (1 << depth) / kSfWarps;
+            wbase = tl.off((int32_t)w * per);
+            int32_t o = wbase;
+            for (int32_t l = 0; l < per; ++l) {
+                const int32_t nn = tl.size((int32_t)w * per + l);
+                for (int32_t q = (int32_t)lane; q < nn; q += 32) pcur[(o + q) & (int32_t)tmask] = (uint8_t)l;
+                o += nn;
+            }
+            __syncwarp();
         }
         for (; j + 4 < S.L; ++j) {
             const int depth = j - a.l0;
@@ -541,28 +561,91 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
             const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
             const int32_t per = cnt / kSfWarps;
             const int32_t ib = (int32_t)w * per;
-            const int drr = j % k;
-            int32_t off = wbase;  // node i's segment, packed from wbase
-            for (int32_t i = ib; i < ib + per; ++i) {
-                const int32_t nn = tl.size(i), m = tl.msize(i);
-                const int d = a.mode == KDT_SPLIT_ROUND_ROBIN ? drr : sf_widest_dim(a, sm, s0, depth, i);
-                const int32_t lo_l = off - (i - ib);
-                sf_split_sorted(a, sm, A + d * T + off, 0u, (uint32_t)nn, (uint32_t)m, Bq + d * T + lo_l,
-                                Bq + d * T + lo_l + m, base, depth, first + i, i, d);
-                __syncwarp();
-                for (int c = 0; c < k; ++c) {
-                    if (c == d) continue;
-                    const uint32_t fin = sf_split_other(A + c * T + off, 0u, (uint32_t)nn, sm.side, Bq + c * T + lo_l,
-                                                        Bq + c * T + lo_l + m, 0u, 0u, tmask);
-                    if (fin != ((uint32_t)m | ((uint32_t)(nn - 1 - m) << 16)) && lane == 0)
-                        set_status(a.status, KDT_EINTERNAL);
+            if (per > 32) {  // cannot happen for T <= 4096; keeps the shuffles in range
+                if (lane == 0) set_status(a.status, KDT_EINTERNAL);
+                break;
+            }
+            // lane l: constants of the warp's node l
+            int32_t nn_l = 0, m_l = 0, d_l = 0;
+            if ((int32_t)lane < per) {
+                nn_l = tl.size(ib + (int32_t)lane);
+                m_l = tl.msize(ib + (int32_t)lane);
+                d_l = a.mode == KDT_SPLIT_ROUND_ROBIN ? j % k : sf_widest_dim(a, sm, s0, depth, ib + (int32_t)lane);
+            }
+            int32_t st_l = nn_l, lb_l = m_l;  // inclusive scans, then exclusive
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int32_t x = __shfl_up_sync(0xffffffffu, st_l, o2), y = __shfl_up_sync(0xffffffffu, lb_l, o2);
+                if ((int32_t)lane >= o2) {
+                    st_l += x;
+                    lb_l += y;
                 }
-                off += nn;
+            }
+            const int32_t live_w = __shfl_sync(0xffffffffu, st_l, 31), lefts = __shfl_sync(0xffffffffu, lb_l, 31);
+            st_l -= nn_l;
+            lb_l -= m_l;
+            const uint32_t pk1 = (uint32_t)st_l | ((uint32_t)m_l << 16);
+            const uint32_t pk2 = (uint32_t)lb_l | ((uint32_t)d_l << 16);
+            // the array of each node's split dimension: sides by offset
+            for (int32_t q0 = 0; q0 < live_w; q0 += 32) {
+                const int32_t q = q0 + (int32_t)lane;
+                const bool v = q < live_w;
+                const uint32_t nd = v ? pcur[(wbase + q) & (int32_t)tmask] & 31u : 0u;
+                const uint32_t a1 = __shfl_sync(0xffffffffu, pk1, nd), a2 = __shfl_sync(0xffffffffu, pk2, nd);
+                if (v) {
+                    const int32_t st = (int32_t)(a1 & 0xffffu), m = (int32_t)(a1 >> 16), d = (int32_t)(a2 >> 16);
+                    const int32_t r = q - st;  // rank in the node's order on d
+                    const uint32_t id = A[d * T + ((wbase + q) & (int32_t)tmask)] & tmask;
+                    const int32_t cb = st - (int32_t)nd;  // the children's segments start here
+                    if (r == m) {
+                        sm.side[id] = 2u;
+                        sf_emit(a, sm, base, depth, first + ib + (int32_t)nd, ib + (int32_t)nd, id, d);
+                    } else {
+                        const bool right = r > m;
+                        sm.side[id] = right ? 1u : 0u;
+                        const int32_t dst = (wbase + cb + (right ? r - 1 : r)) & (int32_t)tmask;
+                        Bq[d * T + dst] = (uint16_t)id;
+                        pnxt[dst] = (uint8_t)(2u * nd + (right ? 1u : 0u));
+                    }
+                }
+            }
+            __syncwarp();
+            // the other arrays: stable partition by side flags
+            for (int c = 0; c < k; ++c) {
+                if (a.mode == KDT_SPLIT_ROUND_ROBIN && c == j % k) continue;
+                uint32_t lp = 0u, rp = 0u;
+                const uint32_t lt = (1u << lane) - 1u;
+                for (int32_t q0 = 0; q0 < live_w; q0 += 32) {
+                    const int32_t q = q0 + (int32_t)lane;
+                    const bool v = q < live_w;
+                    const uint32_t nd = v ? pcur[(wbase + q) & (int32_t)tmask] & 31u : 0u;
+                    const uint32_t a1 = __shfl_sync(0xffffffffu, pk1, nd), a2 = __shfl_sync(0xffffffffu, pk2, nd);
+                    uint32_t id = 0u, s = 3u;
+                    if (v) {
+                        id = A[c * T + ((wbase + q) & (int32_t)tmask)] & tmask;
+                        s = sm.side[id];
+                    }
+                    const uint32_t lb = __ballot_sync(0xffffffffu, s == 0u), rb = __ballot_sync(0xffffffffu, s == 1u);
+                    // a node split on c itself was moved by the pass above: counted, not stored
+                    if (s < 2u && (int32_t)(a2 >> 16) != c) {
+                        const int32_t st = (int32_t)(a1 & 0xffffu), m = (int32_t)(a1 >> 16), lbn = (int32_t)(a2 & 0xffffu);
+                        const int32_t dst = s == 0u ? (int32_t)(lp + __popc(lb & lt)) + (st - (int32_t)nd - lbn)
+                                                    : (int32_t)(rp + __popc(rb & lt)) + lbn + m;
+                        Bq[c * T + ((wbase + dst) & (int32_t)tmask)] = (uint16_t)id;
+                    }
+                    lp += __popc(lb);
+                    rp += __popc(rb);
+                }
+                if (lane == 0 && (lp != (uint32_t)lefts || rp != (uint32_t)(live_w - per - lefts)))
+                    set_status(a.status, KDT_EINTERNAL);
             }
             __syncwarp();
             uint16_t *t2 = A;
             A = Bq;
             Bq = t2;
+            uint8_t *t3 = pcur;
+            pcur = pnxt;
+            pnxt = t3;
         }
     }
 

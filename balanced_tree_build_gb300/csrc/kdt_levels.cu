@@ -34,7 +34,7 @@ namespace kdt {
 constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
 constexpr int kEPT = 4;                          // consecutive points per thread per tile
-constexpr int kPartThreads = 256;                // partition CTAs (multi-CTA and per-subtree)
+constexpr int kPartThreads = 128;                // partition CTAs (multi-CTA and per-subtree)
 constexpr int kPre = 4;                          // key columns loaded ahead in a tile
 constexpr int kTile = kPartThreads * kEPT;
 
@@ -551,7 +551,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
     return pp;
 }
 
-__global__ void __launch_bounds__(kPartThreads, 4) level_part_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a) {
     __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
 
 // ---- one CTA per subtree -------------------------------------------------------
 
-__global__ void __launch_bounds__(kPartThreads, 4) level_seg_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a) {
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t red[64];
@@ -686,7 +686,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        const int64_t grid = (int64_t)sms * 4;  // four partition CTAs per SM stay resident
+        const int64_t grid = (int64_t)sms * 8;  // eight partition CTAs per SM stay resident
         a.per_cta = (live + grid - 1) / grid;
         const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
         const bool fused_here = l > 0 && fusable;
