@@ -25,12 +25,13 @@
 //      the array of its split coordinate, then every array is partitioned
 //      stably into the children's segments (ballot compaction; a count pass
 //      gives each warp its start);
-//   4. lower levels: each warp owns whole subtrees and partitions them node by
-//      node the same way, without CTA barriers;
-//   5. level L-3 (nodes of 3..7 points): one lane per node reads the node's
-//      split point, then each child's points in the order of the child's split
-//      coordinate, which fixes the child and its two leaves.  Tiles that start
-//      lower finish with the same reads on level L-2 or L-1.
+//   4. lower levels: each warp owns whole subtrees (at most 8 nodes per
+//      level) and splits each array in one pass over its range, without CTA
+//      barriers: a byte per position names its node, whose constants come by
+//      shuffle from the lane that holds them;
+//   5. subtrees of at most 15 points (levels >= L-4): one lane each; every
+//      node of the subtree scans the subtree's points in the order of its
+//      split coordinate, keeps those carrying its code and ranks them.
 //
 // Segments of a level are laid out as in the select finisher: node i of the
 // level (counted from the tile's first node on it) starts at the sum of the
