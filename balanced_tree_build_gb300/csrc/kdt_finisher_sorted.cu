@@ -1,6 +1,6 @@
 // kdt_finisher_sorted.cu -- the presorted shared-memory finisher: one CTA
 // owns a subtree of at most T points and fixes all of its remaining levels on
-// chip, with one sort per dimension and then stable partitions.
+// chip, with one sort per dimension and then in-place partitions.
 //
 // Method.  "An Implementation of a Balanced Kd Tree Builder Using GPUs"
 // (overview list, after Brown's O(kn log n) builder): sort one reference
@@ -12,6 +12,20 @@
 // Construction of Left-Balanced k-d Trees", problem paragraph), so the tree is
 // the same one the level-by-level method builds.
 //
+// Layout: in-order.  The tile's subtree is itself a left-balanced complete
+// tree of n nodes (height h, Mt nodes on its last level), and every array
+// keeps the points of a live node u in the range of in-order positions that
+// u's subtree will occupy: [lo(u), lo(u) + ss(u)).  Sorted by its split
+// coordinate, that range already reads [left subtree | u | right subtree], so
+// u's split point sits at its final in-order position pos(u) = lo(u) +
+// ss(lChild(u)) in the array of its own split coordinate, which therefore
+// never moves on u's level.  Only the other arrays are partitioned: left
+// points to [lo(u), pos(u)), the split point to pos(u), right points after
+// it.  Fixed points are never touched again, so after the last level every
+// position p holds the point of the node whose in-order position is p.
+// The in-order position <-> node maps of a left-balanced tree have closed
+// forms (below), so no node table is stored.
+//
 // Per tile (subtree s0 of level l0, n <= T points):
 //   1. load the k coordinate keys and the input index of its points;
 //   2. for each coordinate c, order the local ids by the super key of c: a
@@ -20,43 +34,25 @@
 //      super key.  A bucket of more than kSfMaxBucket points (heavy ties or
 //      clustered values) leaves the whole tile to the select finisher, which
 //      handles any input;
-//   3. levels with fewer nodes than warps: a group of warps per node.  The
-//      node's points are marked left / median / right from their offsets in
-//      the array of its split coordinate, then every array is partitioned
-//      stably into the children's segments (ballot compaction; a count pass
-//      gives each warp its start);
-//   4. lower levels: each warp owns whole subtrees (at most 8 nodes per
-//      level) and splits each array in one pass over its range, without CTA
-//      barriers: a byte per position names its node, whose constants come by
-//      shuffle from the lane that holds them;
-//   5. subtrees of at most 15 points (levels >= L-4): one lane each; every
-//      node of the subtree scans the subtree's points in the order of its
-//      split coordinate, keeps those carrying its code and ranks them.
-//
-// Segments of a level are laid out as in the select finisher: node i of the
-// level (counted from the tile's first node on it) starts at the sum of the
-// sizes of nodes 0..i-1, children follow their parents' order, so the left
-// child of node i starts at off(i) - i.
+//   3. level by level (8 consecutive positions per thread): side flags
+//      (left / split / right) of every live point from the array of its
+//      node's split coordinate; then each array that a later level still
+//      needs is partitioned in place: each thread holds its 8 ids in
+//      registers, a segmented count over the CTA (segments = node ranges,
+//      left and right counts packed in one word) gives every point its
+//      destination;
+//   4. output: node u reads its point at pos(u) of an array that is final
+//      there, and writes perm[u] (coalesced: threads walk level order).
 #include "kdt_internal.cuh"
 #include "kdt_select.cuh"
 
 namespace kdt {
 
-constexpr int kSfThreads = 512;
-constexpr int kSfWarps = kSfThreads / 32;
-constexpr int kSfPPT = 8;          // points per thread in the sort (T <= kSfPPT * kSfThreads)
+constexpr int kSfPPT = 8;          // positions (sort points) per thread: T = kSfPPT * threads
 constexpr int kSfMaxBucket = 16;   // larger buckets leave the tile to the select finisher
-constexpr size_t kSfSmemBudget = 110 * 1024;  // two CTAs per SM
+constexpr size_t kSfSmemBudget = 110 * 1024;  // two 512-thread CTAs per SM
 constexpr int kMaxLevels = 32;
-
-// Constants of level j of the whole tree (B = 2^(L-1-j), notation of the
-// closed forms for ss and sb): with level index jv = s - F(j),
-//   ss(s) = B-1 + clamp(M - jv*B, 0, B), so the first q = M / B subtrees of
-//   the level hold 2B-1 points, subtree q holds B-1+rem (rem = M - q*B) and
-//   the rest B-1.
-struct SfLevel {
-    int32_t B, q, rem;
-};
+constexpr uint32_t kSegHead = 0x80000000u;  // scan word: a node range starts inside the scanned span
 
 struct SfArgs {
     Shape S;
@@ -67,15 +63,16 @@ struct SfArgs {
     const float *dom;    // node table of level l0 (widest mode)
     uint8_t *fallback;   // per tile: 1 = left to the select finisher
     int *status;
-    SfLevel lv[kMaxLevels];
 };
 
 static size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Dynamic shared memory of one CTA: reference arrays [k][T] u16, keys [k][T]
-// u32 (after the sort: the second reference array set and the side flags),
-// input indices [T], nb 16-bit bucket counters, a [T] u16 bucket staging array, and
-// in widest mode the split value and dimension of every tile node.
+// u32 (after the sort: the partition increment of each point), input indices
+// [T], nb >= T 16-bit bucket counters (after the sort: the node ranges of a
+// level), a [T] u16 bucket staging array (after the sort, in widest mode: the
+// split dimension of each node of a level), and in widest mode the split
+// value and dimension of every tile node.
 size_t sorted_finisher_smem(int k, int T, int mode, int nb) {
     size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)2 * nb + (size_t)2 * T;
     if (mode == KDT_SPLIT_WIDEST) b += (size_t)5 * T;
@@ -83,30 +80,32 @@ size_t sorted_finisher_smem(int k, int T, int mode, int nb) {
 }
 
 struct SfSmem {
-    uint16_t *ids0;   // [k][T]
+    uint16_t *ids;    // [k][T]
     uint32_t *keys;   // [k][T], live during the sort
-    uint16_t *ids1;   // [k][T], aliases keys after the sort
-    uint8_t *side;    // [T], aliases keys + 2kT bytes after the sort
+    uint32_t *side;   // [T] partition increment per point, aliases keys after the sort
     uint32_t *idx;    // [T]
     uint32_t *hist;   // [nb / 2]: two 16-bit bucket counters per word
+    uint32_t *ntab;   // [T/4] node ranges of a level (lo | pos << 16), aliases hist after the sort
     uint16_t *stage;  // [T] points grouped by bucket, before ranking
+    uint8_t *ldim;    // [T/2] split dimension per node of a level, aliases stage (widest mode)
     float *sval;      // [T] split value of tile node (widest mode)
     uint8_t *sdim;    // [T] split dimension of tile node (widest mode)
 };
 
 __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int nb) {
     SfSmem f;
-    f.ids0 = reinterpret_cast<uint16_t *>(p);
+    f.ids = reinterpret_cast<uint16_t *>(p);
     p += (size_t)2 * k * T;
     f.keys = reinterpret_cast<uint32_t *>(p);
-    f.ids1 = reinterpret_cast<uint16_t *>(p);
-    f.side = p + (size_t)2 * k * T;
+    f.side = reinterpret_cast<uint32_t *>(p);
     p += (size_t)4 * k * T;
     f.idx = reinterpret_cast<uint32_t *>(p);
     p += (size_t)4 * T;
     f.hist = reinterpret_cast<uint32_t *>(p);
+    f.ntab = f.hist;
     p += (size_t)2 * nb;
     f.stage = reinterpret_cast<uint16_t *>(p);
+    f.ldim = p;
     p += (size_t)2 * T;
     f.sval = reinterpret_cast<float *>(p);
     p += (size_t)4 * T;
@@ -127,36 +126,31 @@ __device__ __forceinline__ bool sk_less_tail(const uint32_t *keys, const uint32_
     return idx[a] < idx[b];
 }
 
-// Level j of the tile whose first node on level j has level index jv0:
-// sizes, left-child sizes and offsets of its nodes i = 0..cnt-1.
-struct TileLevel {
-    int32_t B, q, rem, half, M, jv0, S0;
+// ---- in-order closed forms of the tile's left-balanced shape -------------------
+// The tile holds n nodes: levels 0..h-2 full, level h-1 holding the first Mt
+// of its 2^(h-1) slots.  In the perfect tree of height h the in-order position
+// P of the node at level l, index i is (2i+1)*2^(h-1-l) - 1 and its subtree
+// starts at i*2^(h-l); the last-level slots that are empty are the even
+// positions P >= 2*Mt, so an actual position p maps to P = p below 2*Mt and
+// to P = 2p - 2Mt + 1 above it.
 
-    __device__ __forceinline__ int32_t Sf(int32_t J) const { return B * min(J, q) + (J > q ? rem : 0); }
-    __device__ __forceinline__ int32_t size(int32_t i) const {
-        int32_t r = M - (jv0 + i) * B;
-        r = r < 0 ? 0 : (r > B ? B : r);
-        return B - 1 + r;
-    }
-    // ss(lChild(u)) for node i
-    __device__ __forceinline__ int32_t msize(int32_t i) const {
-        int32_t r = M - (jv0 + i) * B;
-        r = r < 0 ? 0 : (r > half ? half : r);
-        return half - 1 + r;
-    }
-    __device__ __forceinline__ int32_t off(int32_t i) const { return i * (B - 1) + Sf(jv0 + i) - S0; }
-};
+// 1-based level-order index (root 1) of the node at in-order position p < n.
+__device__ __forceinline__ uint32_t io_node1(uint32_t p, int h, uint32_t Mt) {
+    const uint32_t P = p < 2u * Mt ? p : 2u * p - 2u * Mt + 1u;
+    const int b = __ffs((int)(P + 1u)) - 1;
+    return (1u << (h - 1 - b)) + ((P + 1u) >> (b + 1));
+}
 
-__device__ __forceinline__ TileLevel make_tile_level(const Shape &S, const SfLevel &c, int j, int64_t first) {
-    TileLevel t;
-    t.B = c.B;
-    t.q = c.q;
-    t.rem = c.rem;
-    t.half = c.B >> 1;
-    t.M = (int32_t)S.M;
-    t.jv0 = (int32_t)(first - full_nodes(j));
-    t.S0 = t.Sf(t.jv0);
-    return t;
+// In-order position of node i of level l.
+__device__ __forceinline__ uint32_t io_pos(uint32_t i, int l, int h, uint32_t Mt) {
+    const uint32_t P = ((2u * i + 1u) << (h - 1 - l)) - 1u;
+    return P < 2u * Mt ? P : (P + 2u * Mt - 1u) >> 1;
+}
+
+// First in-order position of the subtree of node i of level l.
+__device__ __forceinline__ uint32_t io_lo(uint32_t i, int l, int h, uint32_t Mt) {
+    const uint32_t P = i << (h - l);
+    return P < 2u * Mt ? P : (P >> 1) + Mt;
 }
 
 // Split dimension of tile node i on relative depth `depth` under the widest
@@ -185,174 +179,42 @@ __device__ int sf_widest_dim(const SfArgs &a, const SfSmem &sm, int64_t s0, int 
     return widest_dim(lo, hi, k);
 }
 
-__device__ __forceinline__ int sf_dim(const SfArgs &a, const SfSmem &sm, int64_t s0, int j, int32_t i) {
-    return a.mode == KDT_SPLIT_ROUND_ROBIN ? j % a.k : sf_widest_dim(a, sm, s0, j - a.l0, i);
-}
-
-// Node i (level-order id u, relative depth `depth`) takes local point `id`,
-// split on dimension d, as its split point.
-__device__ __forceinline__ void sf_emit(const SfArgs &a, const SfSmem &sm, int64_t base, int depth, int64_t u,
-                                        int32_t i, uint32_t id, int d) {
-    a.perm[u] = (int32_t)sm.idx[id];
-    if (a.mode == KDT_SPLIT_WIDEST) {
-        const int32_t lu = ((1 << depth) - 1) + i;  // < n: tile nodes exist left to right
-        if (lu < a.T) {
-            sm.sval[lu] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + id));
-            sm.sdim[lu] = (uint8_t)d;
-        }
-    }
-}
-
-// CTA-wide min and max (every thread gets both); `red` holds 2 * kSfWarps words.
+// CTA-wide min and max (every thread gets both); `red` holds 2 * NW words.
+template <int NW>
 __device__ __forceinline__ void sf_block_minmax(uint32_t &mn, uint32_t &mx, uint32_t *red) {
     mn = __reduce_min_sync(0xffffffffu, mn);
     mx = __reduce_max_sync(0xffffffffu, mx);
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (lane == 0) {
         red[w] = mn;
-        red[kSfWarps + w] = mx;
+        red[NW + w] = mx;
     }
     __syncthreads();
-    mn = __reduce_min_sync(0xffffffffu, lane < (uint32_t)kSfWarps ? red[lane] : 0xffffffffu);
-    mx = __reduce_max_sync(0xffffffffu, lane < (uint32_t)kSfWarps ? red[kSfWarps + lane] : 0u);
+    mn = __reduce_min_sync(0xffffffffu, lane < (uint32_t)NW ? red[lane] : 0xffffffffu);
+    mx = __reduce_max_sync(0xffffffffu, lane < (uint32_t)NW ? red[NW + lane] : 0u);
     __syncthreads();
 }
 
-// Warp: the split of a node on the array of its split coordinate, whose
-// segment `seg` lists the node's points in that order.  The points at
-// offsets [qb, qe) go to their child in the same order (offset < m: left
-// child, dl[offset]; offset > m: right child, dr[offset - m - 1]), their side
-// flags are set (0 left, 1 right, 2 split point) and the split point is
-// emitted.  Local ids are masked to the tile (T a power of two), so corrupt
-// data cannot address outside it; the per-node counts of the other arrays
-// catch it.
-__device__ __forceinline__ void sf_split_sorted(const SfArgs &a, const SfSmem &sm, const uint16_t *seg, uint32_t qb,
-                                                uint32_t qe, uint32_t m, uint16_t *dl, uint16_t *dr, int64_t base,
-                                                int depth, int64_t u, int32_t i, int d) {
-    const uint32_t tmask = (uint32_t)a.T - 1u;
-    for (uint32_t q = qb + lane_id(); q < qe; q += 32) {
-        const uint32_t id = seg[q] & tmask;
-        sm.side[id] = (uint8_t)(q < m ? 0u : (q == m ? 2u : 1u));
-        if (q < m) dl[q] = (uint16_t)id;
-        else if (q > m) dr[(q - m - 1u) & tmask] = (uint16_t)id;
-        else sf_emit(a, sm, base, depth, u, i, id, d);
-    }
+// Segmented sum: `cur` continues the range of `prev` unless a range starts in
+// it (kSegHead); the flag of either side survives in bit 31 (values < 2^29).
+__device__ __forceinline__ uint32_t seg_combine(uint32_t prev, uint32_t cur) {
+    return (cur & kSegHead) ? cur : prev + cur;
 }
 
-// Warp: numbers of left and right points at offsets [qb, qe) of `seg` (qb a
-// multiple of 32), packed as left | right << 16.
-__device__ __forceinline__ uint32_t sf_count_other(const uint16_t *seg, uint32_t qb, uint32_t qe,
-                                                   const uint8_t *side, uint32_t tmask) {
-    uint32_t l = 0u, r = 0u;
-    for (uint32_t q0 = qb; q0 < qe; q0 += 32) {
-        const uint32_t q = q0 + lane_id();
-        const uint32_t s = q < qe ? side[seg[q] & tmask] : 2u;
-        l += __popc(__ballot_sync(0xffffffffu, s == 0u));
-        r += __popc(__ballot_sync(0xffffffffu, s == 1u));
-    }
-    return l | (r << 16);
+// Local id number e of the 8 packed in v.
+__device__ __forceinline__ uint32_t ids_at(const uint4 &v, int e) {
+    const uint32_t wv = e < 2 ? v.x : (e < 4 ? v.y : (e < 6 ? v.z : v.w));
+    return (e & 1) ? (wv >> 16) : (wv & 0xffffu);
 }
 
-// Warp: stable partition of the points at offsets [qb, qe) of `seg` by
-// their side flags: left points to dl[lp...], right points to dr[rp...] in
-// their order (lp, rp: points of the node placed by earlier offsets).
-// Returns the final lp | rp << 16.  Destinations are masked to the tile.
-__device__ __forceinline__ uint32_t sf_split_other(const uint16_t *seg, uint32_t qb, uint32_t qe,
-                                                   const uint8_t *side, uint16_t *dl, uint16_t *dr, uint32_t lp,
-                                                   uint32_t rp, uint32_t tmask) {
-    const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;
-    for (uint32_t q0 = qb; q0 < qe; q0 += 32) {
-        const uint32_t q = q0 + lane;
-        uint32_t id = 0u, s = 2u;
-        if (q < qe) {
-            id = seg[q] & tmask;
-            s = side[id];
-        }
-        const uint32_t lb = __ballot_sync(0xffffffffu, s == 0u);
-        const uint32_t rb = __ballot_sync(0xffffffffu, s == 1u);
-        if (s < 2u) {
-            uint16_t *dst = s == 0u ? dl + ((lp + __popc(lb & lt)) & tmask) : dr + ((rp + __popc(rb & lt)) & tmask);
-            *dst = (uint16_t)id;
-        }
-        lp += __popc(lb);
-        rp += __popc(rb);
-    }
-    return lp | (rp << 16);
-}
-
-// One lane: the whole subtree of node u (level j, index irel on its tile
-// level, nn <= 15 points at offset o of every array).  code[id] (the side
-// array) is the local level-order index (root 0) of the subtree node that
-// holds point id.  Each local node scans the subtree's points in the order of
-// its split coordinate, keeps those with its code and ranks them: rank
-// ss(lChild) is its split point, lower ranks take the left child's code,
-// higher ones the right child's.  A node of at most 3 points emits its
-// children (single points) directly.
-__device__ void sf_finish_small(const SfArgs &a, const SfSmem &sm, int64_t s0, int64_t base, int j, int64_t u,
-                                int32_t irel, int32_t o, int32_t nn, const uint16_t *A) {
-    const Shape &S = a.S;
-    const int T = a.T, k = a.k;
-    const uint32_t tmask = (uint32_t)T - 1u;
-    uint8_t *code = sm.side;
-    if (nn < 1 || nn > 15 || o < 0 || o + nn > T) {
-        set_status(a.status, KDT_EINTERNAL);
-        return;
-    }
-    for (int32_t q = 0; q < nn; ++q) code[A[o + q] & tmask] = 0;
-    uint32_t done = 0u;  // local nodes already emitted by their parent
-    const int32_t M = (int32_t)S.M;
-    const int d0 = j % k;
-    for (int v = 0; v < 15; ++v) {
-        if ((done >> v) & 1u) continue;
-        const int lev = 31 - __clz(v + 1);
-        const int jj = j + lev;
-        if (jj >= S.L) break;
-        const int32_t vl = v + 1 - (1 << lev);
-        const int64_t uv = ((u + 1) << lev) - 1 + vl;
-        if (uv >= S.N) continue;
-        // ss(uv) and ss(lChild(uv)) from the level's constants (32-bit: uv < 2^31)
-        const int32_t B = a.lv[jj].B, half = B >> 1;
-        const int32_t rm = M - ((int32_t)uv - ((1 << jj) - 1)) * B;
-        const int32_t nv = B - 1 + (rm < 0 ? 0 : (rm > B ? B : rm));
-        const int32_t mv = jj + 1 < S.L ? half - 1 + (rm < 0 ? 0 : (rm > half ? half : rm)) : 0;
-        const int32_t iv = (irel << lev) + vl;
-        int d;
-        if (a.mode == KDT_SPLIT_ROUND_ROBIN) {
-            d = d0 + lev;
-            while (d >= k) d -= k;
-        } else {
-            d = sf_widest_dim(a, sm, s0, jj - a.l0, iv);
-        }
-        const bool leaves = nv <= 3;
-        if (leaves && v < 7) done |= 3u << (2 * v + 1);
-        const uint16_t *seg = A + d * T + o;
-        int32_t r = 0;
-        for (int32_t q = 0; q < nn; ++q) {
-            const uint32_t id = seg[q] & tmask;
-            if (code[id] != (uint8_t)v) continue;
-            if (r == mv) {
-                sf_emit(a, sm, base, jj - a.l0, uv, iv, id, d);
-                code[id] = 0xff;
-            } else if (leaves) {
-                const int64_t c = r < mv ? 2 * uv + 1 : 2 * uv + 2;
-                if (c < S.N) a.perm[c] = (int32_t)sm.idx[id];
-                else set_status(a.status, KDT_EINTERNAL);
-                code[id] = 0xff;
-            } else {
-                code[id] = (uint8_t)(r < mv ? 2 * v + 1 : 2 * v + 2);
-            }
-            ++r;
-        }
-        if (r != nv) set_status(a.status, KDT_EINTERNAL);
-    }
-}
-
-__global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __grid_constant__ SfArgs a) {
+template <int NT, bool RR>
+__global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __grid_constant__ SfArgs a) {
+    constexpr int NW = NT / 32, E = kSfPPT;
     extern __shared__ __align__(16) unsigned char sf_smem[];
-    __shared__ uint32_t red[2 * kSfWarps];
-    __shared__ uint32_t wcnt[kSfWarps][kMaxK];
+    __shared__ uint32_t red[64];
+    __shared__ uint32_t wagg[2][NW];  // [round parity][warp]: segmented warp sums
     __shared__ int stop;
-    const uint32_t tid = threadIdx.x, NT = kSfThreads;
+    const uint32_t tid = threadIdx.x;
     const uint32_t w = tid >> 5, lane = tid & 31u;
     if (tid == 0) stop = *(volatile int *)a.status;
     __syncthreads();
@@ -366,7 +228,7 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
     const int64_t s0 = full_nodes(a.l0) + blockIdx.x;
     const uint32_t n = (uint32_t)seg_size(S, a.l0, s0);
     const int64_t base = seg_begin(S, a.l0, s0);
-    if (n > (uint32_t)T || (uint32_t)T > kSfPPT * NT || (uint32_t)nb % (2u * NT) != 0u || nb > 65536) {
+    if (n < 1u || n > (uint32_t)T || T != E * NT || (uint32_t)nb % (2u * NT) != 0u || nb > 65536) {
         if (tid == 0) {
             set_status(a.status, KDT_EINTERNAL);
             a.fallback[blockIdx.x] = 0;
@@ -399,7 +261,7 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
             mn = min(mn, v);
             mx = max(mx, v);
         }
-        sf_block_minmax(mn, mx, red);
+        sf_block_minmax<NW>(mn, mx, red);
         const float lo = key2f(mn);
         const float rg = __fsub_rn(key2f(mx), lo);
         float scale = 0.f;
@@ -414,9 +276,9 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
         }
         for (uint32_t b = tid; b < (uint32_t)nb / 2u; b += NT) sm.hist[b] = 0u;
         __syncthreads();
-        uint32_t pk[kSfPPT];
+        uint32_t pk[E];
 #pragma unroll
-        for (int i = 0; i < kSfPPT; ++i) {
+        for (int i = 0; i < E; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
             pk[i] = 0u;
             if (q < n) {
@@ -447,15 +309,15 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < kSfPPT; ++i) {
+        for (int i = 0; i < E; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
             if (q < n) sm.stage[h16[pk[i] >> 16] + (pk[i] & 0xffffu)] = (uint16_t)q;
         }
         __syncthreads();
         // rank inside the bucket under the super key of c
-        uint16_t *arr = sm.ids0 + c * T;
+        uint16_t *arr = sm.ids + c * T;
 #pragma unroll
-        for (int i = 0; i < kSfPPT; ++i) {
+        for (int i = 0; i < E; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
             if (q < n) {
                 const uint32_t b = pk[i] >> 16;
@@ -479,208 +341,192 @@ __global__ void __launch_bounds__(kSfThreads, 2) sorted_finisher_kernel(const __
     if (tid == 0) a.fallback[blockIdx.x] = fail ? 1 : 0;
     if (fail) return;
 
-    // 3. levels with fewer nodes than warps: a group of warps per node
+    // 3. levels.  Thread tid owns in-order positions p0 .. p0+7; g[e] is the
+    //    1-based level-order index (tile-local) of the node whose final
+    //    position is p0+e (0 past the tile).  On level l the position is live
+    //    if that node's level is >= l; its node on level l is then
+    //    g >> (level - l), and the next bit of g says left or right.
+    //    side[id] holds the point's count increment for the partition: 1
+    //    (left), 1 << 16 (right) or 0 (split point).
     const uint32_t tmask = (uint32_t)T - 1u;
-    uint16_t *A = sm.ids0, *Bq = sm.ids1;
-    int j = a.l0;
-    for (; j + 4 < S.L; ++j) {
-        const int depth = j - a.l0;
-        const int32_t cnt = 1 << depth;  // levels <= L-2 are full
-        if (cnt >= kSfWarps) break;
-        const int64_t first = ((s0 + 1) << depth) - 1;
-        const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
-        const uint32_t wpg = (uint32_t)(kSfWarps / cnt);
-        const int32_t i = (int32_t)(w / wpg);
-        const uint32_t r = w % wpg, g0 = w - r;
-        const int32_t off = tl.off(i), nn = tl.size(i), m = tl.msize(i);
-        const int d = sf_dim(a, sm, s0, j, i);
-        const uint32_t nch = ((uint32_t)nn + 31u) / 32u;
-        const uint32_t qb = min(32u * (r * nch / wpg), (uint32_t)nn);
-        const uint32_t qe = min(32u * ((r + 1u) * nch / wpg), (uint32_t)nn);
-        const int32_t lo_l = off - i;
-        sf_split_sorted(a, sm, A + d * T + off, qb, qe, (uint32_t)m, Bq + d * T + lo_l, Bq + d * T + lo_l + m, base,
-                        depth, first + i, i, d);
-        __syncthreads();
-        for (int c = 0; c < k; ++c) {
-            if (c == d) continue;
-            const uint32_t v = sf_count_other(A + c * T + off, qb, qe, sm.side, tmask);
-            if (lane == 0) wcnt[w][c] = v;
-        }
-        __syncthreads();
-        for (int c = 0; c < k; ++c) {
-            if (c == d) continue;
-            const uint32_t pre = __reduce_add_sync(0xffffffffu, lane < r ? wcnt[g0 + lane][c] : 0u);
-            const uint32_t fin = sf_split_other(A + c * T + off, qb, qe, sm.side, Bq + c * T + lo_l,
-                                                Bq + c * T + lo_l + m, pre & 0xffffu, pre >> 16, tmask);
-            if (r == wpg - 1u && fin != ((uint32_t)m | ((uint32_t)(nn - 1 - m) << 16)) && lane == 0)
-                set_status(a.status, KDT_EINTERNAL);
-        }
-        __syncthreads();
-        uint16_t *t2 = A;
-        A = Bq;
-        Bq = t2;
-    }
-
-    // 4. lower levels: warp w owns nodes [w*cnt/W, (w+1)*cnt/W) of every
-    //    level.  Its subtrees stay packed from the offset `wbase` where it
-    //    took them over: in the tile-wide layout a warp's range moves left
-    //    level by level (split points leave) and would reach ranges that a
-    //    slower neighbour still reads.  A warp owns at most 8 nodes per level
-    //    here (this phase starts with one node per warp and ends at level L-5
-    //    of tiles of at most 4096 points), so lane l holds the constants of
-    //    its l-th node -- start of its segment, ss(lChild), left points of the
-    //    nodes before it, split dimension -- and every position finds them by
-    //    one shuffle from the byte that names its node (written when the
-    //    point moved to its child on the level above).  Each array is then
-    //    split in one pass over the warp's range, with no per-node loops: the
-    //    array of a node's split dimension by offset, the others by side flag
-    //    and running left/right counts (left point: Lpre + right points of
-    //    the earlier nodes; right point: Rpre + their left points + m).
-    bool warp_owned = false;
-    int32_t wbase = 0;
-    if (j + 4 < S.L) {
-        warp_owned = true;
-        uint8_t *pcur = reinterpret_cast<uint8_t *>(sm.stage), *pnxt = pcur + T;  // warp-local node of each position
-        {
-            const int depth = j - a.l0;
-            const int64_t first = ((s0 + 1) << depth) - 1;
-            const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
-            const int32_t per = (1 << depth) / kSfWarps;
-            wbase = tl.off((int32_t)w * per);
-            int32_t o = wbase;
-            for (int32_t l = 0; l < per; ++l) {
-                const int32_t nn = tl.size((int32_t)w * per + l);
-                for (int32_t q = (int32_t)lane; q < nn; q += 32) pcur[(o + q) & (int32_t)tmask] = (uint8_t)l;
-                o += nn;
-            }
-            __syncwarp();
-        }
-        for (; j + 4 < S.L; ++j) {
-            const int depth = j - a.l0;
-            const int32_t cnt = 1 << depth;
-            const int64_t first = ((s0 + 1) << depth) - 1;
-            const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
-            const int32_t per = cnt / kSfWarps;
-            const int32_t ib = (int32_t)w * per;
-            if (per > 32) {  // cannot happen for T <= 4096; keeps the shuffles in range
-                if (lane == 0) set_status(a.status, KDT_EINTERNAL);
-                break;
-            }
-            // lane l: constants of the warp's node l
-            int32_t nn_l = 0, m_l = 0, d_l = 0;
-            if ((int32_t)lane < per) {
-                nn_l = tl.size(ib + (int32_t)lane);
-                m_l = tl.msize(ib + (int32_t)lane);
-                d_l = a.mode == KDT_SPLIT_ROUND_ROBIN ? j % k : sf_widest_dim(a, sm, s0, depth, ib + (int32_t)lane);
-            }
-            int32_t st_l = nn_l, lb_l = m_l;  // inclusive scans, then exclusive
+    constexpr bool rr = RR;
+    const int h = 32 - __clz((int)n);
+    const uint32_t Mt = n - ((1u << (h - 1)) - 1u);
+    const uint32_t p0 = tid * (uint32_t)E;
+    const bool wact = w * 32u * (uint32_t)E < n;  // the warp holds a position of the tile
+    uint32_t g[E];
 #pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                const int32_t x = __shfl_up_sync(0xffffffffu, st_l, o2), y = __shfl_up_sync(0xffffffffu, lb_l, o2);
-                if ((int32_t)lane >= o2) {
-                    st_l += x;
-                    lb_l += y;
-                }
+    for (int e = 0; e < E; ++e) g[e] = p0 + e < n ? io_node1(p0 + e, h, Mt) : 0u;
+    const uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? io_node1(p0 - 1u, h, Mt) : 0u;
+    const int last = h - 2;  // deepest level that moves an array
+    if (!rr) {
+        if (tid == 0) sm.ldim[0] = (uint8_t)sf_widest_dim(a, sm, s0, 0, 0);
+        __syncthreads();
+    }
+    const uint32_t allk = (1u << k) - 1u;  // k <= KDT_MAX_K < 32
+    int dl0 = rr ? a.l0 % k : 0;           // round-robin split coordinate of level l
+    int par = 0;
+    for (int l = 0; l <= last; ++l, dl0 = dl0 + 1 == k ? 0 : dl0 + 1) {
+        // arrays to partition on this level: round-robin -- those that some
+        // level in (l, last] splits on (the last - l coordinates after dl0,
+        // cyclically), except this level's own; widest -- all (a node's own
+        // split array is skipped per point)
+        uint32_t mv = allk;
+        if (rr) {
+            const int m = last - l;
+            if (m < k - 1) {
+                const uint32_t run = ((1u << m) - 1u) << (dl0 + 1);  // bits dl0+1 .. dl0+m, unwrapped
+                mv = (run | (run >> k)) & allk;
             }
-            const int32_t live_w = __shfl_sync(0xffffffffu, st_l, 31), lefts = __shfl_sync(0xffffffffu, lb_l, 31);
-            st_l -= nn_l;
-            lb_l -= m_l;
-            const uint32_t pk1 = (uint32_t)st_l | ((uint32_t)m_l << 16);
-            const uint32_t pk2 = (uint32_t)lb_l | ((uint32_t)d_l << 16);
-            // the array of each node's split dimension: sides by offset
-            for (int32_t q0 = 0; q0 < live_w; q0 += 32) {
-                const int32_t q = q0 + (int32_t)lane;
-                const bool v = q < live_w;
-                const uint32_t nd = v ? pcur[(wbase + q) & (int32_t)tmask] & 31u : 0u;
-                const uint32_t a1 = __shfl_sync(0xffffffffu, pk1, nd), a2 = __shfl_sync(0xffffffffu, pk2, nd);
-                if (v) {
-                    const int32_t st = (int32_t)(a1 & 0xffffu), m = (int32_t)(a1 >> 16), d = (int32_t)(a2 >> 16);
-                    const int32_t r = q - st;  // rank in the node's order on d
-                    const uint32_t id = A[d * T + ((wbase + q) & (int32_t)tmask)] & tmask;
-                    const int32_t cb = st - (int32_t)nd;  // the children's segments start here
-                    if (r == m) {
-                        sm.side[id] = 2u;
-                        sf_emit(a, sm, base, depth, first + ib + (int32_t)nd, ib + (int32_t)nd, id, d);
-                    } else {
-                        const bool right = r > m;
-                        sm.side[id] = right ? 1u : 0u;
-                        const int32_t dst = (wbase + cb + (right ? r - 1 : r)) & (int32_t)tmask;
-                        Bq[d * T + dst] = (uint16_t)id;
-                        pnxt[dst] = (uint8_t)(2u * nd + (right ? 1u : 0u));
-                    }
-                }
-            }
-            __syncwarp();
-            // the other arrays: stable partition by side flags
-            for (int c = 0; c < k; ++c) {
-                if (a.mode == KDT_SPLIT_ROUND_ROBIN && c == j % k) continue;
-                uint32_t lp = 0u, rp = 0u;
-                const uint32_t lt = (1u << lane) - 1u;
-                for (int32_t q0 = 0; q0 < live_w; q0 += 32) {
-                    const int32_t q = q0 + (int32_t)lane;
-                    const bool v = q < live_w;
-                    const uint32_t nd = v ? pcur[(wbase + q) & (int32_t)tmask] & 31u : 0u;
-                    const uint32_t a1 = __shfl_sync(0xffffffffu, pk1, nd), a2 = __shfl_sync(0xffffffffu, pk2, nd);
-                    uint32_t id = 0u, s = 3u;
-                    if (v) {
-                        id = A[c * T + ((wbase + q) & (int32_t)tmask)] & tmask;
-                        s = sm.side[id];
-                    }
-                    const uint32_t lb = __ballot_sync(0xffffffffu, s == 0u), rb = __ballot_sync(0xffffffffu, s == 1u);
-                    // a node split on c itself was moved by the pass above: counted, not stored
-                    if (s < 2u && (int32_t)(a2 >> 16) != c) {
-                        const int32_t st = (int32_t)(a1 & 0xffffu), m = (int32_t)(a1 >> 16), lbn = (int32_t)(a2 & 0xffffu);
-                        const int32_t dst = s == 0u ? (int32_t)(lp + __popc(lb & lt)) + (st - (int32_t)nd - lbn)
-                                                    : (int32_t)(rp + __popc(rb & lt)) + lbn + m;
-                        Bq[c * T + ((wbase + dst) & (int32_t)tmask)] = (uint16_t)id;
-                    }
-                    lp += __popc(lb);
-                    rp += __popc(rb);
-                }
-                if (lane == 0 && (lp != (uint32_t)lefts || rp != (uint32_t)(live_w - per - lefts)))
-                    set_status(a.status, KDT_EINTERNAL);
-            }
-            __syncwarp();
-            uint16_t *t2 = A;
-            A = Bq;
-            Bq = t2;
-            uint8_t *t3 = pcur;
-            pcur = pnxt;
-            pnxt = t3;
+            mv &= ~(1u << dl0);
+            if (mv == 0u) break;  // k >= 2: only for l >= h-2; k == 1: never moves
         }
+        // this level's node ranges: lo | pos << 16 per node
+        for (uint32_t i = tid; i < (1u << l); i += NT) sm.ntab[i] = io_lo(i, l, h, Mt) | (io_pos(i, l, h, Mt) << 16);
+        // live / head masks: a node range starts at p if p is live and p-1
+        // is not (p-1 holds a fixed ancestor, or p == 0)
+        uint32_t live = 0u, head = 0u;
+        if (wact) {
+            uint32_t gp = gprev;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const bool lv = g[e] != 0u && 31 - __clz((int)g[e]) >= l;
+                const bool pl = gp != 0u && 31 - __clz((int)gp) >= l;
+                live |= (uint32_t)lv << e;
+                head |= (uint32_t)(lv && !pl) << e;
+                gp = g[e];
+            }
+            if (p0 == 0u) head |= live & 1u;
+            // phase A: side increments from the split arrays
+            if (rr) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(sm.ids + dl0 * T + p0);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (!((live >> e) & 1u)) continue;
+                    const int dl = (31 - __clz((int)g[e])) - l;
+                    const uint32_t inc = dl == 0 ? 0u : (((g[e] >> (dl - 1)) & 1u) ? 0x10000u : 1u);
+                    sm.side[ids_at(v, e) & tmask] = inc;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (!((live >> e) & 1u)) continue;
+                    const int dl = (31 - __clz((int)g[e])) - l;
+                    const uint32_t ga = g[e] >> dl;
+                    const int d = sm.ldim[ga - (1u << l)];
+                    const uint32_t id = sm.ids[d * T + p0 + e] & tmask;
+                    sm.side[id] = dl == 0 ? 0u : (((g[e] >> (dl - 1)) & 1u) ? 0x10000u : 1u);
+                    if (dl == 0) {
+                        const uint32_t ib = id < n ? id : 0u;  // a permutation of [0, n) unless corrupt
+                        sm.sval[ga - 1u] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + ib));
+                        sm.sdim[ga - 1u] = (uint8_t)d;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // phases B and D, one array at a time (B of the next array may run
+        // while slower warps finish D of this one: different arrays, and the
+        // warp sums alternate between two buffers)
+        uint32_t rest = mv;
+        while (rest != 0u) {
+            const int c = __ffs((int)rest) - 1;
+            rest &= rest - 1u;
+            uint4 iv = make_uint4(0u, 0u, 0u, 0u);
+            uint32_t X[E], mask = 0u, exw = 0u;
+            // B: running left | right << 16 counts before each held point,
+            // from its range start (kSegHead set) or from p0; warp scan
+            if (wact) {
+                iv = *reinterpret_cast<const uint4 *>(sm.ids + c * T + p0);
+                mask = live;
+                if (!rr) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if (!((live >> e) & 1u)) continue;
+                        const int dl = (31 - __clz((int)g[e])) - l;
+                        if (sm.ldim[(g[e] >> dl) - (1u << l)] == c) mask &= ~(1u << e);  // own split array
+                    }
+                }
+                uint32_t run = 0u;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if ((head >> e) & 1u) run = kSegHead;
+                    X[e] = run;
+                    if ((mask >> e) & 1u) run += sm.side[ids_at(iv, e) & tmask];
+                }
+                uint32_t x = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= (uint32_t)o) x = seg_combine(y, x);
+                }
+                if (lane == 31u) wagg[par][w] = x;
+                const uint32_t ex = __shfl_up_sync(0xffffffffu, x, 1);
+                exw = lane == 0u ? 0u : ex;
+            }
+            __syncthreads();
+            // D: carry from the warps before, destinations, in-place stores
+            if (wact) {
+                uint32_t v = lane < (uint32_t)NW ? wagg[par][lane] : 0u;
+#pragma unroll
+                for (int o = 1; o < NW; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= (uint32_t)o) v = seg_combine(y, v);
+                }
+                const uint32_t cw = __shfl_sync(0xffffffffu, v, (w + 31u) & 31u);
+                const uint32_t lb = (exw & kSegHead) ? (exw & ~kSegHead) : (w > 0u ? (cw & ~kSegHead) : 0u) + exw;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (!((mask >> e) & 1u)) continue;
+                    const uint32_t id = ids_at(iv, e);
+                    const uint32_t inc = sm.side[id & tmask];
+                    const uint32_t val = (X[e] & kSegHead) ? (X[e] & ~kSegHead) : lb + X[e];
+                    const int dl = (31 - __clz((int)g[e])) - l;
+                    const uint32_t nt = sm.ntab[(g[e] >> dl) - (1u << l)];
+                    const uint32_t pos = nt >> 16;
+                    const uint32_t dst = inc == 1u ? (nt & 0xffffu) + (val & 0xffffu)
+                                                   : (inc == 0u ? pos : pos + 1u + (val >> 16));
+                    if (dst < n) sm.ids[c * T + dst] = (uint16_t)id;
+                    else set_status(a.status, KDT_EINTERNAL);
+                }
+            }
+            par ^= 1;
+        }
+        // widest: split dimensions of the next level's nodes (their
+        // ancestors' split values were recorded in phase A)
+        if (!rr && l + 1 <= last) {
+            for (uint32_t i = tid; i < (1u << (l + 1)); i += NT) sm.ldim[i] = (uint8_t)sf_widest_dim(a, sm, s0, l + 1, (int32_t)i);
+        }
+        __syncthreads();
     }
 
-    // 5. subtrees of at most 15 points (levels >= L-4): one lane each
-    {
-        const int depth = j - a.l0;
-        const int32_t cnt = 1 << depth;
-        const int64_t first = ((s0 + 1) << depth) - 1;
-        const int64_t count = min((int64_t)cnt, S.N - first);  // nodes that exist
-        const TileLevel tl = make_tile_level(S, a.lv[j], j, first);
-        // CTA-wide: tile-wide layout; warp-owned: this warp's own nodes,
-        // packed from wbase, and no CTA barrier needed
-        int32_t ie = (int32_t)count, step = (int32_t)NT, i0 = (int32_t)tid, shift = 0;
-        if (warp_owned) {
-            const int32_t ib = (int32_t)w * (cnt / kSfWarps);
-            ie = ib + cnt / kSfWarps;
-            step = 32;
-            i0 = ib + (int32_t)lane;
-            shift = wbase - tl.off(ib);
+    // 4. output: node u of the tile (level lv, index i) reads its point at
+    //    pos(u) from an array that is final there -- in round-robin mode the
+    //    array of its own level's split coordinate (leaves: the one of level
+    //    h-2), in widest mode any (all arrays move on every level)
+    for (uint32_t u = tid; u < n; u += NT) {
+        const uint32_t g1 = u + 1u;
+        const int lv = 31 - __clz((int)g1);
+        const uint32_t i = g1 - (1u << lv);
+        const uint32_t p = io_pos(i, lv, h, Mt);
+        if (p >= n) {
+            set_status(a.status, KDT_EINTERNAL);
+            continue;
         }
-        for (int32_t i = i0; i < ie; i += step) {
-            const int64_t u = first + i;
-            sf_finish_small(a, sm, s0, base, j, u, i, tl.off(i) + shift, (int32_t)seg_size(S, j, u), A);
-        }
+        const int c = rr ? (a.l0 + min(lv, max(last, 0))) % k : 0;
+        const uint32_t id = sm.ids[c * T + p] & tmask;
+        a.perm[((s0 + 1) << lv) - 1 + i] = (int32_t)sm.idx[id];
     }
 }
 
-// Tile size T: the largest candidate whose sorted-finisher CTA fits two per
-// SM and whose select-finisher CTA (the fallback for the same tiles) fits one.
+// Tile size T: the largest candidate whose sorted-finisher CTA (T / 8
+// threads) fits two per SM and whose select-finisher CTA (the fallback for the
+// same tiles) fits one.
 int pick_tile(int k, int mode, TilePlan *tp) {
     static const int cands[] = {4096, 2048, 1024, 512};
     for (int T : cands) {
-        if (T > kSfPPT * kSfThreads) continue;
-        const int nb = T > 2 * kSfThreads ? T : 2 * kSfThreads;  // about one point per bucket
+        const int threads = T / kSfPPT;
+        const int nb = T > 2 * threads ? T : 2 * threads;  // about one point per bucket
         const size_t a = sorted_finisher_smem(k, T, mode, nb);
         const size_t b = select_finisher_smem(k, T, mode);
         if (a <= kSfSmemBudget && b <= kSelectSmemMax) {
@@ -692,6 +538,21 @@ int pick_tile(int k, int mode, TilePlan *tp) {
         }
     }
     return -1;
+}
+
+template <int NT, bool RR>
+static int launch_sorted_mode(const SfArgs &a, int64_t ntiles, size_t smem, cudaStream_t stream) {
+    if (cudaFuncSetAttribute(sorted_finisher_kernel<NT, RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return KDT_ECUDA;
+    sorted_finisher_kernel<NT, RR><<<(unsigned)ntiles, NT, smem, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ECUDA;
+}
+
+template <int NT>
+static int launch_sorted(const SfArgs &a, int64_t ntiles, size_t smem, cudaStream_t stream) {
+    return a.mode == KDT_SPLIT_ROUND_ROBIN ? launch_sorted_mode<NT, true>(a, ntiles, smem, stream)
+                                           : launch_sorted_mode<NT, false>(a, ntiles, smem, stream);
 }
 
 int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream) {
@@ -711,26 +572,20 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.dom = b.dom[p.finish_level & 1];
     a.fallback = b.fallback;
     a.status = b.status;
-    for (int j = 0; j < kMaxLevels; ++j) {
-        SfLevel &c = a.lv[j];
-        c = SfLevel{};
-        if (j >= S.L) continue;
-        const int lgB = S.L - 1 - j;
-        const int64_t B = (int64_t)1 << lgB, q = S.M >> lgB;
-        c.B = (int32_t)B;
-        c.q = (int32_t)q;
-        c.rem = (int32_t)(S.M - q * B);
-    }
-    if (cudaFuncSetAttribute(sorted_finisher_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)p.tp.smem) != cudaSuccess)
-        return KDT_ECUDA;
     const int64_t ntiles = nodes_on_level(S, p.finish_level);
     const double Nd = (double)S.N;
     const double sort_levels = (double)(S.L - 1 - p.finish_level);
     {
         ProfScope ps(stream, "finisher", 20.0 * (Nd - (double)full_nodes(p.finish_level)) * sort_levels + 12.0 * Nd);
-        sorted_finisher_kernel<<<(unsigned)ntiles, kSfThreads, p.tp.smem, stream>>>(a);
-        if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        int rc;
+        switch (a.T / kSfPPT) {
+            case 512: rc = launch_sorted<512>(a, ntiles, p.tp.smem, stream); break;
+            case 256: rc = launch_sorted<256>(a, ntiles, p.tp.smem, stream); break;
+            case 128: rc = launch_sorted<128>(a, ntiles, p.tp.smem, stream); break;
+            case 64: rc = launch_sorted<64>(a, ntiles, p.tp.smem, stream); break;
+            default: rc = KDT_EINVAL;
+        }
+        if (rc != KDT_OK) return rc;
     }
     ProfScope ps(stream, "finisher_select", 0.0);
     return launch_select_finisher(p, b, src, perm, b.fallback, stream);
