@@ -215,6 +215,20 @@ __device__ __forceinline__ void load4(const uint32_t *col, int64_t q0, uint32_t 
     v[3] = x.w;
 }
 
+// Prefetches the record lines of the tile starting at t0 (a multiple of 4,
+// clipped to ve) into L2, so that the tile's loads, issued one tile later,
+// wait on L2 rather than DRAM: one 128-byte line per thread and column.
+__device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve) {
+    const uint32_t lines = kTile / 32;  // 128-byte lines per column
+    for (uint32_t t = threadIdx.x; t < (uint32_t)(a.k + 1) * lines; t += blockDim.x) {
+        const uint32_t c = t / lines;
+        const int64_t q = t0 + (int64_t)(t - c * lines) * 32;
+        if (q >= ve) continue;
+        const uint32_t *col = (int)c < a.k ? a.src_keys + (int64_t)c * a.ld : a.src_idx;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(col + q));
+    }
+}
+
 // Partitions the points of [vb, ve) that fall in the tile starting at t0 (a
 // multiple of 4): thread t handles positions t0 + 4t .. t0 + 4t + 3.
 // `cursors` points at three counters (left, candidate, right) in shared or
@@ -575,8 +589,10 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a
             for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
         }
         __syncthreads();
-        for (int64_t t0 = p & ~(int64_t)3; t0 < pe; t0 += kTile)
+        for (int64_t t0 = p & ~(int64_t)3; t0 < pe; t0 += kTile) {
+            if (t0 + kTile < pe) prefetch_tile(a, t0 + kTile, pe);
             part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
+        }
         __syncthreads();
         if (fuse) {
             uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
@@ -640,8 +656,10 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     Bucketer none;
     none.lo = 0.f;
     none.scale = 0.f;
-    for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile)
+    for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile) {
+        if (t0 + kTile < g.base + (int64_t)g.n) prefetch_tile(a, t0 + kTile, g.base + (int64_t)g.n);
         part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
+    }
     __syncthreads();
     if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
