@@ -343,9 +343,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
 
     // 3. levels.  Thread tid owns in-order positions p0 .. p0+7; g[e] is the
     //    1-based level-order index (tile-local) of the node whose final
-    //    position is p0+e (0 past the tile).  On level l the position is live
-    //    if that node's level is >= l; its node on level l is then
-    //    g >> (level - l), and the next bit of g says left or right.
+    //    position is p0+e, followed by a terminating one bit and shifted left
+    //    until its leading one is bit 31 (0 past the tile): bit 30 - j is then
+    //    the side taken below level j.  On level l, t = g << (l + 1) is 0 if
+    //    the position is fixed (the node's level is < l), exactly bit 31 for
+    //    the node of level l itself (its split point), and otherwise has the
+    //    side in bit 31; the node on level l has index g >> (31 - l).
     //    side[id] holds the point's count increment for the partition: 1
     //    (left), 1 << 16 (right) or 0 (split point).
     const uint32_t tmask = (uint32_t)T - 1u;
@@ -356,8 +359,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     const bool wact = w * 32u * (uint32_t)E < n;  // the warp holds a position of the tile
     uint32_t g[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) g[e] = p0 + e < n ? io_node1(p0 + e, h, Mt) : 0u;
-    const uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? io_node1(p0 - 1u, h, Mt) : 0u;
+    for (int e = 0; e < E; ++e) {
+        const uint32_t u1 = p0 + e < n ? io_node1(p0 + e, h, Mt) : 0u;
+        g[e] = u1 ? ((u1 << 1) | 1u) << (__clz((int)u1) - 1) : 0u;
+    }
+    uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? io_node1(p0 - 1u, h, Mt) : 0u;
+    gprev = gprev ? ((gprev << 1) | 1u) << (__clz((int)gprev) - 1) : 0u;
     const int last = h - 2;  // deepest level that moves an array
     if (!rr) {
         if (tid == 0) sm.ldim[0] = (uint8_t)sf_widest_dim(a, sm, s0, 0, 0);
@@ -387,14 +394,13 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         // is not (p-1 holds a fixed ancestor, or p == 0)
         uint32_t live = 0u, head = 0u;
         if (wact) {
-            uint32_t gp = gprev;
+            bool pl = (gprev << (l + 1)) != 0u;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                const bool lv = g[e] != 0u && 31 - __clz((int)g[e]) >= l;
-                const bool pl = gp != 0u && 31 - __clz((int)gp) >= l;
+                const bool lv = (g[e] << (l + 1)) != 0u;
                 live |= (uint32_t)lv << e;
                 head |= (uint32_t)(lv && !pl) << e;
-                gp = g[e];
+                pl = lv;
             }
             if (p0 == 0u) head |= live & 1u;
             // phase A: side increments from the split arrays
@@ -403,20 +409,19 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     if (!((live >> e) & 1u)) continue;
-                    const int dl = (31 - __clz((int)g[e])) - l;
-                    const uint32_t inc = dl == 0 ? 0u : (((g[e] >> (dl - 1)) & 1u) ? 0x10000u : 1u);
-                    sm.side[ids_at(v, e) & tmask] = inc;
+                    const uint32_t t = g[e] << (l + 1);
+                    sm.side[ids_at(v, e) & tmask] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
                 }
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     if (!((live >> e) & 1u)) continue;
-                    const int dl = (31 - __clz((int)g[e])) - l;
-                    const uint32_t ga = g[e] >> dl;
-                    const int d = sm.ldim[ga - (1u << l)];
+                    const uint32_t t = g[e] << (l + 1);
+                    const uint32_t ga = g[e] >> (31 - l);
+                    const int d = sm.ldim[ga ^ (1u << l)];
                     const uint32_t id = sm.ids[d * T + p0 + e] & tmask;
-                    sm.side[id] = dl == 0 ? 0u : (((g[e] >> (dl - 1)) & 1u) ? 0x10000u : 1u);
-                    if (dl == 0) {
+                    sm.side[id] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
+                    if (t == 0x80000000u) {
                         const uint32_t ib = id < n ? id : 0u;  // a permutation of [0, n) unless corrupt
                         sm.sval[ga - 1u] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + ib));
                         sm.sdim[ga - 1u] = (uint8_t)d;
@@ -443,8 +448,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         if (!((live >> e) & 1u)) continue;
-                        const int dl = (31 - __clz((int)g[e])) - l;
-                        if (sm.ldim[(g[e] >> dl) - (1u << l)] == c) mask &= ~(1u << e);  // own split array
+                        if (sm.ldim[(g[e] >> (31 - l)) ^ (1u << l)] == c) mask &= ~(1u << e);  // own split array
                     }
                 }
                 uint32_t run = 0u;
@@ -481,8 +485,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                     const uint32_t id = ids_at(iv, e);
                     const uint32_t inc = sm.side[id & tmask];
                     const uint32_t val = (X[e] & kSegHead) ? (X[e] & ~kSegHead) : lb + X[e];
-                    const int dl = (31 - __clz((int)g[e])) - l;
-                    const uint32_t nt = sm.ntab[(g[e] >> dl) - (1u << l)];
+                    const uint32_t nt = sm.ntab[(g[e] >> (31 - l)) ^ (1u << l)];
                     const uint32_t pos = nt >> 16;
                     const uint32_t dst = inc == 1u ? (nt & 0xffffu) + (val & 0xffffu)
                                                    : (inc == 0u ? pos : pos + 1u + (val >> 16));
