@@ -427,45 +427,70 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
     const uint32_t lane = tid & 31u, lt = (1u << lane) - 1u;
     const uint32_t nright = pp.cnt - 1u - r;
     const int64_t right_begin = g.left_begin + g.m;
-    for (uint32_t q0 = 0; q0 < pp.cnt; q0 += nt) {
-        const uint32_t q = q0 + tid;
-        int side = -1;
-        if (q < pp.cnt) {
-            const int c = cmp_words(acc, q, medw, k + 1);
-            side = c < 0 ? 0 : (c > 0 ? 1 : -1);
+    // up to four candidates per thread and round (one if every thread has at
+    // most one): their first words, and then each column of the moved
+    // records, are loaded before they are used
+    constexpr int kRB = 4;
+    const int rb = pp.cnt > nt ? kRB : 1;
+    for (uint32_t q0 = 0; q0 < pp.cnt; q0 += (uint32_t)rb * nt) {
+        uint32_t w0[kRB];
+#pragma unroll
+        for (int u = 0; u < kRB; ++u) {
+            const uint32_t q = q0 + (uint32_t)u * nt + tid;
+            w0[u] = u < rb && q < pp.cnt ? acc(0, q) : 0u;
         }
-        const uint32_t lm = __ballot_sync(0xffffffffu, side == 0);
-        const uint32_t rm = __ballot_sync(0xffffffffu, side == 1);
-        uint32_t lb = 0, rb = 0;
-        if (lane == 0) {
-            if (lm) lb = atomicAdd(&cur2[0], __popc(lm));
-            if (rm) rb = atomicAdd(&cur2[1], __popc(rm));
-        }
-        lb = __shfl_sync(0xffffffffu, lb, 0);
-        rb = __shfl_sync(0xffffffffu, rb, 0);
-        if (side >= 0) {
-            int64_t pos;
-            bool ok;
-            if (side == 0) {
-                const uint32_t o = lb + __popc(lm & lt);
-                ok = o < r;
-                pos = g.left_begin + pp.below + o;
-            } else {
-                const uint32_t o = rb + __popc(rm & lt);
-                ok = o < nright;
-                pos = right_begin + o;
+        int side[kRB];
+        int64_t pos[kRB], sp[kRB];
+#pragma unroll
+        for (int u = 0; u < kRB; ++u) {
+            const uint32_t q = q0 + (uint32_t)u * nt + tid;
+            side[u] = -1;
+            pos[u] = 0;
+            sp[u] = 0;
+            if (u >= rb) continue;  // uniform: rb is the same in every thread
+            if (q < pp.cnt) {
+                const int c = w0[u] != medw[0] ? (w0[u] < medw[0] ? -1 : 1) : cmp_words(acc, q, medw, k + 1);
+                side[u] = c < 0 ? 0 : (c > 0 ? 1 : -1);
             }
-            if (ok) {
-                const int64_t sp = acc.pos(q);
-                for (int c = 0; c < k; ++c) {
-                    const uint32_t v = a.cand_keys[(int64_t)c * ld + sp];
-                    a.dst_keys[(int64_t)c * ld + pos] = v;
-                    if (fuse && c == dn)
-                        atomicAdd(&a.hist_nxt[(2 * g.j + side) * kBuckets + bkc(v)], 1u);
+            const uint32_t lm = __ballot_sync(0xffffffffu, side[u] == 0);
+            const uint32_t rm = __ballot_sync(0xffffffffu, side[u] == 1);
+            uint32_t lb = 0, rb2 = 0;
+            if (lane == 0) {
+                if (lm) lb = atomicAdd(&cur2[0], __popc(lm));
+                if (rm) rb2 = atomicAdd(&cur2[1], __popc(rm));
+            }
+            lb = __shfl_sync(0xffffffffu, lb, 0);
+            rb2 = __shfl_sync(0xffffffffu, rb2, 0);
+            if (side[u] >= 0) {
+                bool ok;
+                if (side[u] == 0) {
+                    const uint32_t o = lb + __popc(lm & lt);
+                    ok = o < r;
+                    pos[u] = g.left_begin + pp.below + o;
+                } else {
+                    const uint32_t o = rb2 + __popc(rm & lt);
+                    ok = o < nright;
+                    pos[u] = right_begin + o;
                 }
-                a.dst_idx[pos] = a.cand_idx[sp];
-            } else {
-                set_status(a.status, KDT_EINTERNAL);
+                if (ok) {
+                    sp[u] = acc.pos(q);
+                } else {
+                    set_status(a.status, KDT_EINTERNAL);
+                    side[u] = -1;
+                }
+            }
+        }
+        for (int c = 0; c <= k; ++c) {
+            const uint32_t *scol = c < k ? a.cand_keys + (int64_t)c * ld : a.cand_idx;
+            uint32_t *dcol = c < k ? a.dst_keys + (int64_t)c * ld : a.dst_idx;
+            uint32_t v[kRB];
+#pragma unroll
+            for (int u = 0; u < kRB; ++u) v[u] = side[u] >= 0 ? scol[sp[u]] : 0u;
+#pragma unroll
+            for (int u = 0; u < kRB; ++u) {
+                if (side[u] < 0) continue;
+                dcol[pos[u]] = v[u];
+                if (fuse && c == dn) atomicAdd(&a.hist_nxt[(2 * g.j + side[u]) * kBuckets + bkc(v[u])], 1u);
             }
         }
     }

@@ -135,13 +135,42 @@ __device__ __forceinline__ uint32_t value_bucket(uint32_t key, float lo, float s
     return (uint32_t)b < nb ? (uint32_t)b : nb - 1u;
 }
 
-template <class Acc>
-__device__ __forceinline__ bool sel_matches(const Acc &acc, const SelState &st, uint32_t q, uint32_t nb) {
-    if (st.vb_on && value_bucket(acc(0, q), st.vlo, st.vscale, nb) != st.vb) return false;
-    for (int i = 0; i < st.j; ++i)
-        if (acc(i, q) != st.f[i]) return false;
-    if (st.has_prefix && (acc(st.j, q) >> st.sh) != st.pv) return false;
-    return true;
+// Calls f(q, word j of q) for every matching point q of the group's share of
+// [0, n).  Word 0 of eight points is loaded before any of them is tested, so
+// a thread keeps eight loads in flight (the points may sit in global memory);
+// the other words are read only for points that still match.
+template <class G, class Acc, class F>
+__device__ __forceinline__ void for_matching(const G &g, const Acc &acc, const SelState &st, uint32_t n, uint32_t nb,
+                                             F f) {
+    constexpr int kB = 8;
+    const uint32_t tid = g.tid(), nt = g.size();
+    const int j = st.j;
+    auto test = [&](uint32_t q, uint32_t w0) {
+        if (st.vb_on && value_bucket(w0, st.vlo, st.vscale, nb) != st.vb) return;
+        if (j > 0 && w0 != st.f[0]) return;
+        for (int i = 1; i < j; ++i)
+            if (acc(i, q) != st.f[i]) return;
+        const uint32_t wj = j == 0 ? w0 : acc(j, q);
+        if (st.has_prefix && (wj >> st.sh) != st.pv) return;
+        f(q, wj);
+    };
+    if (n <= nt) {  // at most one point per thread: nothing to batch
+        if (tid < n) test(tid, acc(0, tid));
+        return;
+    }
+    for (uint32_t q0 = tid; q0 < n; q0 += kB * nt) {
+        uint32_t w0[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const uint32_t q = q0 + (uint32_t)u * nt;
+            w0[u] = q < n ? acc(0, q) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const uint32_t q = q0 + (uint32_t)u * nt;
+            if (q < n) test(q, w0[u]);
+        }
+    }
 }
 
 // Three-way comparison of point q with the key words w[0..nw).
@@ -184,13 +213,10 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
         if (st.cnt <= 1u || st.j >= nwords) break;
         const int j = st.j;
         uint32_t mn = 0xffffffffu, mx = 0u;
-        for (uint32_t q = tid; q < n; q += nt) {
-            if (sel_matches(acc, st, q, nbins)) {
-                const uint32_t w = acc(j, q);
-                mn = min(mn, w);
-                mx = max(mx, w);
-            }
-        }
+        for_matching(g, acc, st, n, nbins, [&](uint32_t, uint32_t w) {
+            mn = min(mn, w);
+            mx = max(mx, w);
+        });
         group_minmax(g, mn, mx, red);
         if (mn == mx) {
             g.sync();
@@ -224,13 +250,10 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
         }
         for (uint32_t b = tid; b < nbins; b += nt) hist[b] = 0u;
         g.sync();
-        for (uint32_t q = tid; q < n; q += nt) {
-            if (sel_matches(acc, st, q, nbins)) {
-                const uint32_t w = acc(j, q);
-                const uint32_t b = vround ? value_bucket(w, vlo, vscale, nbins) : (w >> sh) - lo;
-                atomicAdd(&hist[b], 1u);
-            }
-        }
+        for_matching(g, acc, st, n, nbins, [&](uint32_t, uint32_t w) {
+            const uint32_t b = vround ? value_bucket(w, vlo, vscale, nbins) : (w >> sh) - lo;
+            atomicAdd(&hist[b], 1u);
+        });
         g.sync();
         const uint32_t per = nbins / nt;
         uint32_t sum = 0;
@@ -271,8 +294,7 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
     }
     if (st.cnt != 1u && tid == 0) st.err = 1;
     g.sync();
-    for (uint32_t q = tid; q < n; q += nt)
-        if (sel_matches(acc, st, q, nbins)) st.med_q = q;
+    for_matching(g, acc, st, n, nbins, [&](uint32_t q, uint32_t) { st.med_q = q; });
     g.sync();
 }
 
