@@ -70,10 +70,12 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
                 }
             }
         }
+        if (idx != nullptr) {
 #pragma unroll
-        for (int u = 0; u < kInitPPT; ++u) {
-            const int64_t i = i0 + u * nt;
-            if (i < N) idx[i] = (uint32_t)i;
+            for (int u = 0; u < kInitPPT; ++u) {
+                const int64_t i = i0 + u * nt;
+                if (i < N) idx[i] = (uint32_t)i;
+            }
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
@@ -193,7 +195,10 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 16;
         if (blocks > cap) blocks = cap;
         ProfScope ps(stream, "init", 0.0);
-        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], b.idx[0], b.bbox,
+        // the input-index column starts as the identity: written only if the
+        // finisher takes the root subtree (global levels use the position)
+        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0],
+                                                                   p.finish_level == 0 ? b.idx[0] : nullptr, b.bbox,
                                                                    b.status);
         KDT_LAUNCH_CHECK();
     }

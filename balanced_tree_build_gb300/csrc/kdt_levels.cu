@@ -216,7 +216,7 @@ __device__ __forceinline__ void load4(const uint32_t *col, int64_t q0, uint32_t 
 }
 
 // Prefetches the record lines of the tile starting at t0 (a multiple of 4,
-// clipped to ve) into L2, so that the tile's loads, issued one tile later,
+// clipped to ve) into L2, so that the tile's loads, issued two tiles later,
 // wait on L2 rather than DRAM: one 128-byte line per thread and column.
 __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve) {
     const uint32_t lines = kTile / 32;  // 128-byte lines per column
@@ -225,6 +225,7 @@ __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, in
         const int64_t q = t0 + (int64_t)(t - c * lines) * 32;
         if (q >= ve) continue;
         const uint32_t *col = (int)c < a.k ? a.src_keys + (int64_t)c * a.ld : a.src_idx;
+        if (col == nullptr) continue;  // level 0: no index column
         asm volatile("prefetch.global.L2 [%0];" ::"l"(col + q));
     }
 }
@@ -255,6 +256,11 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     for (int c = 0; c <= kPre; ++c) {
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) pv[c][i] = 0u;
+        if (c == kPre && a.src_idx == nullptr) {  // level 0: the input index is the position
+#pragma unroll
+            for (int i = 0; i < kEPT; ++i) pv[c][i] = (uint32_t)(q0 + i);
+            continue;
+        }
         if (any && (c == kPre || c < k)) load4(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
     }
     uint32_t kx[kEPT];
@@ -615,7 +621,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a
         }
         __syncthreads();
         for (int64_t t0 = p & ~(int64_t)3; t0 < pe; t0 += kTile) {
-            if (t0 + kTile < pe) prefetch_tile(a, t0 + kTile, pe);
+            if (t0 + 2 * kTile < pe) prefetch_tile(a, t0 + 2 * kTile, pe);
             part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         }
         __syncthreads();
@@ -682,7 +688,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     none.lo = 0.f;
     none.scale = 0.f;
     for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile) {
-        if (t0 + kTile < g.base + (int64_t)g.n) prefetch_tile(a, t0 + kTile, g.base + (int64_t)g.n);
+        if (t0 + 2 * kTile < g.base + (int64_t)g.n) prefetch_tile(a, t0 + 2 * kTile, g.base + (int64_t)g.n);
         part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
     }
     __syncthreads();
@@ -704,7 +710,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.mode = p.mode;
     a.l = l;
     a.src_keys = b.keys[src];
-    a.src_idx = b.idx[src];
+    a.src_idx = l == 0 ? nullptr : b.idx[src];  // level 0 reads no index column: it is the position
     a.dst_keys = b.keys[src ^ 1];
     a.dst_idx = b.idx[src ^ 1];
     a.cand_keys = b.keys[2];
