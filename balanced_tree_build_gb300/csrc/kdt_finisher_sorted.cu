@@ -57,6 +57,7 @@ constexpr uint32_t kSegHead = 0x80000000u;  // scan word: a node range starts in
 struct SfArgs {
     Shape S;
     int k, mode, l0, T, nb;
+    int64_t tile0;       // this launch's first tile (subtree of level l0, counted from the level's first)
     int64_t ld;
     const uint32_t *src_keys, *src_idx;
     int32_t *perm;
@@ -218,20 +219,21 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     const uint32_t w = tid >> 5, lane = tid & 31u;
     if (tid == 0) stop = *(volatile int *)a.status;
     __syncthreads();
+    const int64_t tile = a.tile0 + blockIdx.x;
     if (stop) {
-        if (tid == 0) a.fallback[blockIdx.x] = 0;
+        if (tid == 0) a.fallback[tile] = 0;
         return;
     }
     const Shape &S = a.S;
     const int k = a.k, T = a.T, nb = a.nb;
     const SfSmem sm = sf_carve(sf_smem, k, T, nb);
-    const int64_t s0 = full_nodes(a.l0) + blockIdx.x;
+    const int64_t s0 = full_nodes(a.l0) + tile;
     const uint32_t n = (uint32_t)seg_size(S, a.l0, s0);
     const int64_t base = seg_begin(S, a.l0, s0);
     if (n < 1u || n > (uint32_t)T || T != E * NT || (uint32_t)nb % (2u * NT) != 0u || nb > 65536) {
         if (tid == 0) {
             set_status(a.status, KDT_EINTERNAL);
-            a.fallback[blockIdx.x] = 0;
+            a.fallback[tile] = 0;
         }
         return;
     }
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         }
         __syncthreads();
     }
-    if (tid == 0) a.fallback[blockIdx.x] = fail ? 1 : 0;
+    if (tid == 0) a.fallback[tile] = fail ? 1 : 0;
     if (fail) return;
 
     // 3. levels.  Thread tid owns in-order positions p0 .. p0+7; g[e] is the
@@ -578,17 +580,43 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     const int64_t ntiles = nodes_on_level(S, p.finish_level);
     const double Nd = (double)S.N;
     const double sort_levels = (double)(S.L - 1 - p.finish_level);
+    // Tiles of at most T/2 points run in half-size CTAs (twice as many per
+    // SM).  Subtree sizes on the level do not increase with the index: q
+    // subtrees of 2B-1 points, one of B-1+rem, the rest B-1.
+    const int Ts = a.T / 2;
+    int64_t nbig = ntiles;
+    if (Ts >= 512) {
+        const int lgB = S.L - 1 - p.finish_level;
+        const int64_t B = (int64_t)1 << lgB, q = S.M >> lgB, rem = S.M - (q << lgB);
+        if (B - 1 <= Ts) {
+            nbig = 2 * B - 1 > Ts ? q : 0;
+            if (nbig < ntiles && B - 1 + rem > Ts) ++nbig;
+            if (nbig > ntiles) nbig = ntiles;
+        }
+    }
     {
         ProfScope ps(stream, "finisher", 20.0 * (Nd - (double)full_nodes(p.finish_level)) * sort_levels + 12.0 * Nd);
-        int rc;
-        switch (a.T / kSfPPT) {
-            case 512: rc = launch_sorted<512>(a, ntiles, p.tp.smem, stream); break;
-            case 256: rc = launch_sorted<256>(a, ntiles, p.tp.smem, stream); break;
-            case 128: rc = launch_sorted<128>(a, ntiles, p.tp.smem, stream); break;
-            case 64: rc = launch_sorted<64>(a, ntiles, p.tp.smem, stream); break;
-            default: rc = KDT_EINVAL;
-        }
+        auto launch = [&](const SfArgs &x, int64_t n_tiles, size_t smem) -> int {
+            if (n_tiles <= 0) return KDT_OK;
+            switch (x.T / kSfPPT) {
+                case 512: return launch_sorted<512>(x, n_tiles, smem, stream);
+                case 256: return launch_sorted<256>(x, n_tiles, smem, stream);
+                case 128: return launch_sorted<128>(x, n_tiles, smem, stream);
+                case 64: return launch_sorted<64>(x, n_tiles, smem, stream);
+                default: return KDT_EINVAL;
+            }
+        };
+        a.tile0 = 0;
+        int rc = launch(a, nbig, p.tp.smem);
         if (rc != KDT_OK) return rc;
+        if (nbig < ntiles) {
+            SfArgs b2 = a;
+            b2.T = Ts;
+            b2.nb = Ts;  // about one point per bucket; a multiple of 2 * (Ts / 8) threads
+            b2.tile0 = nbig;
+            rc = launch(b2, ntiles - nbig, sorted_finisher_smem(a.k, Ts, a.mode, Ts));
+            if (rc != KDT_OK) return rc;
+        }
     }
     ProfScope ps(stream, "finisher_select", 0.0);
     return launch_select_finisher(p, b, src, perm, b.fallback, stream);
