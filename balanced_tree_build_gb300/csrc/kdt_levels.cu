@@ -244,13 +244,15 @@ __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, in
 __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
                           int64_t vb, int64_t ve, uint32_t *cursors, uint32_t *wtot, uint32_t *wbase, uint32_t *fh,
                           const Bucketer &bkc, int dn) {
+    // positions are below 2^31 (N < 2^31): 32-bit arithmetic from here on
     const int64_t ld = a.ld;
     const int k = a.k, d = g.d;
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    const int64_t q0 = t0 + 4 * (int64_t)tid;
-    const bool any = q0 + 4 > vb && q0 < ve;
+    const uint32_t q0 = (uint32_t)t0 + 4u * tid;
+    const uint32_t vb32 = (uint32_t)vb, ve32 = (uint32_t)ve;
+    const bool any = q0 + 4u > vb32 && q0 < ve32;
     uint32_t pv[kPre + 1][kEPT];
 #pragma unroll
     for (int c = 0; c <= kPre; ++c) {
@@ -258,7 +260,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         for (int i = 0; i < kEPT; ++i) pv[c][i] = 0u;
         if (c == kPre && a.src_idx == nullptr) {  // level 0: the input index is the position
 #pragma unroll
-            for (int i = 0; i < kEPT; ++i) pv[c][i] = (uint32_t)(q0 + i);
+            for (int i = 0; i < kEPT; ++i) pv[c][i] = q0 + (uint32_t)i;
             continue;
         }
         if (any && (c == kPre || c < k)) load4(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
@@ -282,9 +284,9 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     uint32_t tL = 0, tC = 0, tR = 0;
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
-        const int64_t q = q0 + i;
+        const uint32_t q = q0 + (uint32_t)i;
         int side = 3;
-        if (q >= vb && q < ve) {
+        if (q >= vb32 && q < ve32) {
             const uint32_t b = (uint32_t)bk(kx[i]);
             side = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
         }
@@ -327,8 +329,13 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     }
     __syncthreads();
     uint32_t oL = wbase[3 * w + 0], oC = wbase[3 * w + 1], oR = wbase[3 * w + 2];
+    const uint32_t lbeg = (uint32_t)g.left_begin, rtail = (uint32_t)pp.right_tail;
+    const uint32_t cgap = lbeg + pp.below, s32 = (uint32_t)g.s;
+    // pos: destination position of each point (32 bit); side 3 = not stored;
+    // candidates (side 1, rare) are stored separately below
     uint32_t pos[kEPT];
     int side[kEPT];
+    bool anyc = false;
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         pos[i] = 0u;
@@ -338,18 +345,19 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         if (mL[i] & bit) {
             const uint32_t o = oL + __popc(mL[i] & lt);
             ok = o < pp.below;
-            pos[i] = (uint32_t)(g.left_begin + o);
+            pos[i] = lbeg + o;
             side[i] = 0;
         } else if (mR[i] & bit) {
             const uint32_t o = oR + __popc(mR[i] & lt);
             ok = o < pp.above;
-            pos[i] = (uint32_t)(pp.right_tail + o);
+            pos[i] = rtail + o;
             side[i] = 2;
         } else if (mC[i] & bit) {
             const uint32_t o = oC + __popc(mC[i] & lt);
             ok = o < pp.cnt;
-            pos[i] = (uint32_t)cand_pos(g, pp, o);
+            pos[i] = o + 1u < pp.cnt ? cgap + o : s32;  // the candidate slots (see cand_pos)
             side[i] = 1;
+            anyc = true;
         }
         oL += __popc(mL[i]);
         oC += __popc(mC[i]);
@@ -364,13 +372,18 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     for (int c = 0; c <= kPre; ++c) {
         if (c < kPre && c >= k) continue;
         uint32_t *dcol = c == kPre ? a.dst_idx : a.dst_keys + (int64_t)c * ld;
-        uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * ld;
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
-            if (side[i] == 3) continue;
-            (side[i] == 1 ? ccol : dcol)[pos[i]] = pv[c][i];
-            if (fh != nullptr && c == dn && side[i] != 1)
-                atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
+            if (side[i] == 0 || side[i] == 2) {
+                dcol[pos[i]] = pv[c][i];
+                if (fh != nullptr && c == dn) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
+            }
+        }
+        if (anyc) {
+            uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * ld;
+#pragma unroll
+            for (int i = 0; i < kEPT; ++i)
+                if (side[i] == 1) ccol[pos[i]] = pv[c][i];
         }
     }
     for (int c = kPre; c < k; ++c) {
