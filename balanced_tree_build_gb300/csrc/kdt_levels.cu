@@ -549,6 +549,25 @@ __device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t 
     return total == n;
 }
 
+// Histogram of the bucket function over col[b, e) into shared `hist`; each
+// thread issues eight loads before its atomics (keys are in global memory).
+__device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64_t e, const Bucketer &bk,
+                                           uint32_t *hist) {
+    constexpr int kH = 8;
+    const uint32_t nt = blockDim.x;
+    for (int64_t q0 = b + threadIdx.x; q0 < e; q0 += (int64_t)kH * nt) {
+        uint32_t v[kH];
+#pragma unroll
+        for (int u = 0; u < kH; ++u) {
+            const int64_t q = q0 + (int64_t)u * nt;
+            v[u] = q < e ? __ldg(col + q) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kH; ++u)
+            if (q0 + (int64_t)u * nt < e) atomicAdd(&hist[bk(v[u])], 1u);
+    }
+}
+
 // ---- multi-CTA pipeline kernels ----------------------------------------------
 
 __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
         for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
         const uint32_t *col = a.src_keys + (int64_t)g.d * ld;
-        for (int64_t q = p + threadIdx.x; q < pe; q += blockDim.x) atomicAdd(&hist[bk(col[q])], 1u);
+        hist_range(col, p, pe, bk, hist);
         __syncthreads();
         uint32_t *H = a.hist_cur + g.j * kBuckets;
         for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x)
@@ -688,8 +707,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
     if (threadIdx.x < 3) cursors[threadIdx.x] = 0u;
     __syncthreads();
-    for (int64_t q = g.base + threadIdx.x; q < g.base + (int64_t)g.n; q += blockDim.x)
-        atomicAdd(&hist[bk(col[q])], 1u);
+    hist_range(col, g.base, g.base + (int64_t)g.n, bk, hist);
     __syncthreads();
     const bool ok = pick_bucket(hist, g.n, g.m, red, &pps);
     if (!ok) {
