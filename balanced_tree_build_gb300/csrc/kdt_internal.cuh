@@ -151,6 +151,7 @@ constexpr size_t kSelectSmemMax = 200 * 1024;  // select finisher: at least one 
 struct SegSel {
     uint32_t bstar, below, cnt;
     uint32_t curL, curC, curR;
+    uint32_t klo, khi;  // keys of the split bucket: [klo, khi)
 };
 
 constexpr int kBuckets = 2048;         // value buckets per subtree on global levels

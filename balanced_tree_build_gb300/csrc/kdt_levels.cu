@@ -66,6 +66,25 @@ __device__ __forceinline__ Bucketer make_bucketer(float lo, float hi) {
     return b;
 }
 
+// Finite keys: f2key(-FLT_MAX) .. f2key(FLT_MAX).  Every point's key lies
+// there (non-finite input is rejected), and the bucket function is monotone
+// on that range.
+constexpr uint32_t kKeyMin = 0x00800000u, kKeyMax = 0xff7fffffu;
+
+// Smallest finite key whose bucket is >= b, or kKeyMax + 1 if none: the
+// points of buckets < b are exactly the keys below it (binary search on the
+// monotone bucket function).
+__device__ uint32_t first_key_at_least(const Bucketer &bk, uint32_t b) {
+    if (b >= (uint32_t)kBuckets) return kKeyMax + 1u;
+    uint32_t lo = kKeyMin, hi = kKeyMax + 1u;
+    while (lo < hi) {
+        const uint32_t mid = lo + (hi - lo) / 2u;
+        if ((uint32_t)bk(mid) >= b) hi = mid;
+        else lo = mid + 1u;
+    }
+    return lo;
+}
+
 // Subtree of level l that holds array position p (inverse of sb).
 __device__ __forceinline__ int64_t seg_of_pos(const Shape &S, int l, int64_t p) {
     const int64_t B = (int64_t)1 << (S.L - 1 - l), A = B - 1;
@@ -198,6 +217,7 @@ __device__ __forceinline__ unsigned long long block_scan64(unsigned long long v,
 // position; the others are the gap between the two certain groups).
 struct PartPlan {
     uint32_t bstar, below, cnt, above;
+    uint32_t klo, khi;   // keys of the split bucket b*: [klo, khi)
     int64_t right_tail;  // first position of the certain-right group
 };
 
@@ -286,10 +306,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     for (int i = 0; i < kEPT; ++i) {
         const uint32_t q = q0 + (uint32_t)i;
         int side = 3;
-        if (q >= vb32 && q < ve32) {
-            const uint32_t b = (uint32_t)bk(kx[i]);
-            side = b < pp.bstar ? 0 : (b > pp.bstar ? 2 : 1);
-        }
+        if (q >= vb32 && q < ve32) side = kx[i] < pp.klo ? 0 : (kx[i] >= pp.khi ? 2 : 1);  // bucket vs b*
         mL[i] = __ballot_sync(0xffffffffu, side == 0);
         mC[i] = __ballot_sync(0xffffffffu, side == 1);
         mR[i] = __ballot_sync(0xffffffffu, side == 2);
@@ -603,6 +620,10 @@ __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
     const int64_t s = full_nodes(a.l) + blockIdx.x;
     const SegInfo g = seg_info(a, s);
     const bool ok = pick_bucket(a.hist_cur + g.j * kBuckets, g.n, g.m, red, &pp);
+    // key bounds of the split bucket: two binary searches in two warps
+    if (threadIdx.x == 32) pp.khi = first_key_at_least(seg_bucketer(a, g.j, g.d), pp.bstar + 1u);
+    if (threadIdx.x == 0) pp.klo = first_key_at_least(seg_bucketer(a, g.j, g.d), pp.bstar);
+    __syncthreads();
     if (threadIdx.x == 0) {
         if (!ok) set_status(a.status, KDT_EINTERNAL);
         SegSel sl;
@@ -610,6 +631,8 @@ __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
         sl.below = pp.below;
         sl.cnt = pp.cnt;
         sl.curL = sl.curC = sl.curR = 0u;
+        sl.klo = pp.klo;
+        sl.khi = pp.khi;
         a.sel[g.j] = sl;
     }
     if (a.hist_nxt) {
@@ -618,11 +641,14 @@ __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
     }
 }
 
-__device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, uint32_t below, uint32_t cnt) {
+__device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, uint32_t below, uint32_t cnt,
+                                              uint32_t klo, uint32_t khi) {
     PartPlan pp;
     pp.bstar = bstar;
     pp.below = below;
     pp.cnt = cnt;
+    pp.klo = klo;
+    pp.khi = khi;
     pp.above = g.n - below - cnt;
     pp.right_tail = g.left_begin + g.m + (g.nr - pp.above);
     return pp;
@@ -643,7 +669,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a
         const int64_t pe = min(end, g.base + (int64_t)g.n);
         const Bucketer bk = seg_bucketer(a, g.j, g.d);
         const SegSel sl = a.sel[g.j];
-        const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt);
+        const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt, sl.klo, sl.khi);
         Bucketer bkc;
         bkc.lo = 0.f;
         bkc.scale = 0.f;
@@ -678,7 +704,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
     const int64_t s = full_nodes(a.l) + blockIdx.x;
     const SegInfo g = seg_info(a, s);
     const SegSel sl = a.sel[g.j];
-    const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt);
+    const PartPlan pp = part_plan(g, sl.bstar, sl.below, sl.cnt, sl.klo, sl.khi);
     if (sl.curL != pp.below || sl.curC != pp.cnt || sl.curR != pp.above) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
         return;
@@ -714,7 +740,10 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    const PartPlan pp = part_plan(g, pps.bstar, pps.below, pps.cnt);
+    if (threadIdx.x == 32) pps.khi = first_key_at_least(bk, pps.bstar + 1u);
+    if (threadIdx.x == 0) pps.klo = first_key_at_least(bk, pps.bstar);
+    __syncthreads();
+    const PartPlan pp = part_plan(g, pps.bstar, pps.below, pps.cnt, pps.klo, pps.khi);
     Bucketer none;
     none.lo = 0.f;
     none.scale = 0.f;
