@@ -44,7 +44,7 @@ class KdtError(RuntimeError):
 
 class _KernelStat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64),
-                ("total_ms", ctypes.c_double), ("bytes_alg", ctypes.c_double)]
+                ("total_ms", ctypes.c_double), ("bytes_alg", ctypes.c_double), ("kernels", ctypes.c_int64)]
 
 
 def _load():
@@ -311,5 +311,6 @@ def profile_read() -> list[dict]:
     buf = (_KernelStat * 64)()
     n = L.kdt_profile_read(buf, 64)
     return [{"name": buf[i].name.decode(), "launches": int(buf[i].launches),
-             "total_ms": float(buf[i].total_ms), "bytes_alg": float(buf[i].bytes_alg)}
+             "total_ms": float(buf[i].total_ms), "bytes_alg": float(buf[i].bytes_alg),
+             "kernels": int(buf[i].kernels)}
             for i in range(min(n, 64))]

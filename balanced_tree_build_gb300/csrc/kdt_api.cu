@@ -18,7 +18,10 @@ __global__ void status_fold_kernel(const int *s) {
     if (v != 0) atomicCAS(&g_device_status, 0, v);
 }
 
-void enqueue_status_fold(int *status, cudaStream_t stream) { status_fold_kernel<<<1, 1, 0, stream>>>(status); }
+void enqueue_status_fold(int *status, cudaStream_t stream) {
+    ProfScope ps(stream, "status_fold", 0.0);
+    status_fold_kernel<<<1, 1, 0, stream>>>(status);
+}
 
 int *device_status_address() {
     void *p = nullptr;
@@ -42,12 +45,14 @@ struct Pending {
     const char *name;
     cudaEvent_t ev0, ev1;
     double bytes;
+    int kernels;
 };
 struct Total {
     const char *name;
     int64_t launches;
     double ms;
     double bytes;
+    int64_t kernels;
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -55,7 +60,8 @@ std::vector<Pending> g_pending;
 std::vector<Total> g_totals;
 }  // namespace
 
-ProfScope::ProfScope(cudaStream_t s, const char *n, double b) : stream(s), name(n), bytes(b), ev0(nullptr), on(false) {
+ProfScope::ProfScope(cudaStream_t s, const char *n, double b)
+    : stream(s), name(n), bytes(b), ev0(nullptr), on(false), kernels(1) {
     bool enabled;
     {
         std::lock_guard<std::mutex> g(g_prof_mu);
@@ -76,7 +82,7 @@ ProfScope::~ProfScope() {
     }
     cudaEventRecord(ev1, stream);
     std::lock_guard<std::mutex> g(g_prof_mu);
-    g_pending.push_back({name, ev0, ev1, bytes});
+    g_pending.push_back({name, ev0, ev1, bytes, kernels});
 }
 
 static void drain_pending_locked() {
@@ -92,11 +98,12 @@ static void drain_pending_locked() {
                 t.launches += 1;
                 t.ms += ms;
                 t.bytes += p.bytes;
+                t.kernels += p.kernels;
                 found = true;
                 break;
             }
         }
-        if (!found) g_totals.push_back({p.name, 1, (double)ms, p.bytes});
+        if (!found) g_totals.push_back({p.name, 1, (double)ms, p.bytes, (int64_t)p.kernels});
     }
     g_pending.clear();
 }
@@ -278,6 +285,7 @@ int kdt_profile_read(kdt_kernel_stat *out, int cap) {
         out[i].launches = g_totals[i].launches;
         out[i].total_ms = g_totals[i].ms;
         out[i].bytes_alg = g_totals[i].bytes;
+        out[i].kernels = g_totals[i].kernels;
     }
     return n;
 }

@@ -120,7 +120,9 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     while (lf < q.S.L && seg_size(q.S, lf, full_nodes(lf)) > q.tp.tile) ++lf;
     q.finish_level = lf;
     int lm = 0;
-    while (lm < lf && ((int64_t)1 << lm) <= kMultiMaxSegs && seg_size(q.S, lm, full_nodes(lm)) > kMultiMinSize) ++lm;
+    // every level with few subtrees runs on the whole GPU (multi-CTA); the
+    // one-CTA-per-subtree kernel needs enough subtrees to fill the SMs
+    while (lm < lf && ((int64_t)1 << lm) <= kMultiMaxSegs) ++lm;
     q.multi_levels = lm;
     q.table_cap = (int64_t)1 << lf;
     q.hist_rows = lm > 0 ? ((int64_t)1 << (lm - 1)) : 0;
@@ -202,8 +204,11 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
                                                                    b.status);
         KDT_LAUNCH_CHECK();
     }
-    root_table_kernel<<<1, 1, 0, stream>>>(b.bbox, k, b.dom[0], b.dim[0]);
-    KDT_LAUNCH_CHECK();
+    {
+        ProfScope ps(stream, "root_table", 0.0);
+        root_table_kernel<<<1, 1, 0, stream>>>(b.bbox, k, b.dom[0], b.dim[0]);
+        KDT_LAUNCH_CHECK();
+    }
     int src = 0;
     for (int l = 0; l < p.finish_level; ++l) {
         const int rc = enqueue_level(p, b, l, src, perm, stream);

@@ -607,6 +607,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
             }
         };
         a.tile0 = 0;
+        ps.kernels = (nbig > 0 ? 1 : 0) + (nbig < ntiles ? 1 : 0);
         int rc = launch(a, nbig, p.tp.smem);
         if (rc != KDT_OK) return rc;
         if (nbig < ntiles) {

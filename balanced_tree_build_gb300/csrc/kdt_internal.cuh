@@ -155,8 +155,7 @@ struct SegSel {
 };
 
 constexpr int kBuckets = 2048;         // value buckets per subtree on global levels
-constexpr int kMultiMaxSegs = 1024;    // multi-CTA levels: at most this many subtrees ...
-constexpr int64_t kMultiMinSize = 65536;  // ... each larger than this
+constexpr int kMultiMaxSegs = 1024;    // multi-CTA levels: at most this many subtrees
 
 struct Plan {
     Shape S;
@@ -207,13 +206,15 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
 int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *perm,
                   cudaStream_t stream);
 
-// Per-kernel timing (profiling switch in kdt_api.cu).
+// Per-kernel timing (profiling switch in kdt_api.cu).  `kernels`: kernel
+// launches inside the scope (1 unless the code between the events says so).
 struct ProfScope {
     cudaStream_t stream;
     const char *name;
     double bytes;
     cudaEvent_t ev0;
     bool on;
+    int kernels;
     ProfScope(cudaStream_t s, const char *n, double b);
     ~ProfScope();
 };

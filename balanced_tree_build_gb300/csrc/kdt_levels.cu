@@ -393,7 +393,9 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 0 || side[i] == 2) {
                 dcol[pos[i]] = pv[c][i];
-                if (fh != nullptr && c == dn) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
+                // pv[kPre] is the input index, not key column kPre
+                if (fh != nullptr && c < kPre && c == dn)
+                    atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
             }
         }
         if (anyc) {

@@ -382,7 +382,7 @@ def run_ours(args, workload):
     ms_step = ms_max / args.steps
 
     peak, peak_src = measured_peaks()
-    launches = sum(s["launches"] for s in stats)
+    launches = sum(s["kernels"] for s in stats)  # kernel launches inside the timed scopes
     dom = max(stats, key=lambda s: s["total_ms"]) if stats else None
     roofline = None
     if dom:

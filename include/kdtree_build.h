@@ -180,16 +180,18 @@ int kdt_status(void *stream);
 const char *kdt_error_string(int code);
 
 /* Per-kernel timing.  When enabled, the build records CUDA events around each
- * of its kernel launches (on the build's stream) and accumulates, per kernel
- * family, the launch count and total device time.  kdt_profile_read fills up
- * to `cap` entries (names are static strings) and returns the number of
- * families; it synchronises on the events it reads.  kdt_profile_reset clears
- * the totals.  Off by default. */
+ * of its kernel launches, or around a family's group of launches (on the
+ * build's stream), and accumulates, per kernel family, the number of timed
+ * scopes, their total device time and the kernels launched inside them.
+ * kdt_profile_read fills up to `cap` entries (names are static strings) and
+ * returns the number of families; it synchronises on the events it reads.
+ * kdt_profile_reset clears the totals.  Off by default. */
 typedef struct {
     const char *name;
-    int64_t launches;
+    int64_t launches;  /* timed scopes */
     double total_ms;
-    double bytes_alg; /* algorithmic bytes summed over the launches */
+    double bytes_alg;  /* algorithmic bytes summed over the scopes */
+    int64_t kernels;   /* kernel launches inside those scopes */
 } kdt_kernel_stat;
 
 int kdt_profile_enable(int on);
