@@ -22,9 +22,9 @@
 // child's domain in that dimension is the parent's, so the child's buckets
 // are known while the parent is partitioned.
 //
-// Large subtrees (few per level) are spread over all SMs ("multi-CTA"
+// Levels with at most 1024 subtrees are spread over all SMs ("multi-CTA"
 // pipeline: separate histogram / pick / partition / resolve kernels with
-// per-subtree cursors); once there are many smaller subtrees each CTA owns
+// per-subtree cursors); once there are more subtrees than that each CTA owns
 // one subtree and runs all steps itself ("seg" kernel).
 #include "kdt_internal.cuh"
 #include "kdt_select.cuh"
