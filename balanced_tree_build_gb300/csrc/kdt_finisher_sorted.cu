@@ -21,10 +21,12 @@
 // ss(lChild(u)) in the array of its own split coordinate, which therefore
 // never moves on u's level.  Only the other arrays are partitioned: left
 // points to [lo(u), pos(u)), the split point to pos(u), right points after
-// it.  Fixed points are never touched again, so after the last level every
-// position p holds the point of the node whose in-order position is p.
-// The in-order position <-> node maps of a left-balanced tree have closed
-// forms (below), so no node table is stored.
+// it.  Fixed points are never touched again, so after the last level
+// position p holds the point of the node whose in-order position is p in
+// every array that was partitioned down to that node's level (the output
+// reads such an array).  The in-order position <-> node maps of a
+// left-balanced tree have closed forms (below); the only node table is the
+// current level's node ranges, built from them.
 //
 // Per tile (subtree s0 of level l0, n <= T points):
 //   1. load the k coordinate keys and the input index of its points;
@@ -34,13 +36,13 @@
 //      super key.  A bucket of more than kSfMaxBucket points (heavy ties or
 //      clustered values) leaves the whole tile to the select finisher, which
 //      handles any input;
-//   3. level by level (8 consecutive positions per thread): side flags
-//      (left / split / right) of every live point from the array of its
-//      node's split coordinate; then each array that a later level still
-//      needs is partitioned in place: each thread holds its 8 ids in
-//      registers, a segmented count over the CTA (segments = node ranges,
-//      left and right counts packed in one word) gives every point its
-//      destination;
+//   3. level by level (8 consecutive positions per thread): the side of
+//      every live point (left / split / right, stored as its count
+//      increment) from the array of its node's split coordinate; then each
+//      array that a later level still needs is partitioned in place: each
+//      thread holds its 8 ids in registers, a segmented count over the CTA
+//      (segments = node ranges, left and right counts packed in one word)
+//      gives every point its destination;
 //   4. output: node u reads its point at pos(u) of an array that is final
 //      there, and writes perm[u] (coalesced: threads walk level order).
 #include "kdt_internal.cuh"

@@ -180,34 +180,6 @@ __device__ void write_child_domains(const float *dom_p, int k, int d, float spli
     *dim_r = widest_dim(lo, hi, k);
 }
 
-// Exclusive block scan of a 64-bit value; `total` receives the block sum.
-__device__ __forceinline__ unsigned long long block_scan64(unsigned long long v, unsigned long long *red,
-                                                           unsigned long long &total) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    unsigned long long x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= (uint32_t)o) x += y;
-    }
-    __syncthreads();
-    if (lane == 31) red[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        unsigned long long t = lane < (uint32_t)nw ? red[lane] : 0ull;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= (uint32_t)o) t += y;
-        }
-        red[lane] = t;
-    }
-    __syncthreads();
-    total = red[nw - 1];
-    return (w > 0 ? red[w - 1] : 0ull) + x - v;
-}
-
 // ---- partition of one tile ----------------------------------------------------
 
 // Side of a point relative to the split bucket: 0 left, 1 candidate, 2 right.
@@ -220,10 +192,6 @@ struct PartPlan {
     uint32_t klo, khi;   // keys of the split bucket b*: [klo, khi)
     int64_t right_tail;  // first position of the certain-right group
 };
-
-__device__ __forceinline__ int64_t cand_pos(const SegInfo &g, const PartPlan &pp, uint32_t slot) {
-    return slot + 1u < pp.cnt ? g.left_begin + pp.below + slot : g.s;
-}
 
 // Loads the 4 consecutive words at col[q0 .. q0+4) (q0 a multiple of 4) as
 // one 128-bit load.
@@ -372,7 +340,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         } else if (mC[i] & bit) {
             const uint32_t o = oC + __popc(mC[i] & lt);
             ok = o < pp.cnt;
-            pos[i] = o + 1u < pp.cnt ? cgap + o : s32;  // the candidate slots (see cand_pos)
+            pos[i] = o + 1u < pp.cnt ? cgap + o : s32;  // candidate slot o: the gap, the last one position s
             side[i] = 1;
             anyc = true;
         }
