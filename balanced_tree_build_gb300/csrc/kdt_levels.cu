@@ -418,7 +418,12 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
     const int64_t ld = a.ld;
     const uint32_t r = g.m - pp.below;  // rank of the split point among the candidates
     const CandAcc acc{a.cand_keys, a.cand_idx, ld, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
-    cta_select(acc, pp.cnt, r, k + 1, st, hist, red);
+    if (pp.cnt <= 32u) {  // a few candidates (deep levels): one warp selects, no CTA barriers per round
+        if (tid < 32u) group_select(WarpsGroup{0u, 32u, 1}, acc, pp.cnt, r, k + 1, st, hist, kWarpRadixBits, red);
+        __syncthreads();
+    } else {
+        cta_select(acc, pp.cnt, r, k + 1, st, hist, red);
+    }
     if (st.err) {
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
         return;
