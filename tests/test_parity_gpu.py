@@ -67,6 +67,17 @@ def test_across_tile_boundaries(o, n, k, mode):
     assert_parity(o, make_points("uniform01", n, k, seed=n * 7 + k), mode)
 
 
+@pytest.mark.parametrize("n", [40000, 200003])
+@pytest.mark.parametrize("k", [4, 5, 6, 7, 8, 16])
+@pytest.mark.parametrize("dist", ["uniform01", "dup_heavy"])
+def test_round_robin_many_dims_multi_level(o, n, k, dist):
+    """Round-robin builds whose global levels run on the whole GPU with the
+    next level's histogram fused into the partition: the next split
+    coordinate takes every value 0..k-1, including those past the first
+    four (held apart from the input index in the partition tile)."""
+    assert_parity(o, make_points(dist, n, k, seed=n + 31 * k), 0)
+
+
 @pytest.mark.parametrize("dist", ["all_equal", "dup_heavy", "quant1024", "signed_zero"])
 def test_heavy_ties_multi_level(o, dist):
     assert_parity(o, make_points(dist, 150_000, 3, seed=5), 0)
