@@ -97,19 +97,31 @@ __device__ __forceinline__ float dist2(const float *q, const float *__restrict__
     return d;
 }
 
-// One thread per query.  best_* live in local memory (K <= KDT_MAX_KNN),
-// sorted ascending by (dist2, node).
+// (dd, node) before (d2, n2) in the result order: dist2, then node id.
+__device__ __forceinline__ bool knn_before(float dd, int32_t node, float d2, int32_t n2) {
+    return dd < d2 || (dd == d2 && node < n2);
+}
+
+// One thread per query.  The K best (dist2, node) pairs are kept sorted
+// ascending.  KC > 0: K == KC is known at compile time and the list lives in
+// registers (unrolled insertion); KC == 0: any K <= KDT_MAX_KNN, list in
+// local memory.
+template <int KC>
 __global__ void __launch_bounds__(kQueryThreads) knn_kernel(const float *__restrict__ tree, int64_t N, int k,
                                                             const uint8_t *__restrict__ dims,
                                                             const float *__restrict__ queries, int64_t Q, int K,
                                                             int32_t *out_node, float *out_dist2, int *status) {
+    constexpr int KA = KC > 0 ? KC : KDT_MAX_KNN;
     const int64_t qi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (qi >= Q) return;
+    const int kk = KC > 0 ? KC : K;
     float q[kMaxK];
     for (int c = 0; c < k; ++c) q[c] = __ldg(queries + qi * k + c);
-    float bd[KDT_MAX_KNN];
-    int32_t bn[KDT_MAX_KNN];
-    for (int j = 0; j < K; ++j) {
+    float bd[KA];
+    int32_t bn[KA];
+#pragma unroll
+    for (int j = 0; j < KA; ++j) {
+        if (KC == 0 && j >= kk) break;
         bd[j] = __int_as_float(0x7f800000);  // +infinity
         bn[j] = -1;
     }
@@ -128,14 +140,34 @@ __global__ void __launch_bounds__(kQueryThreads) knn_kernel(const float *__restr
         const int64_t near_c = 2 * cur + (diff < 0.f ? 1 : 2);
         const int64_t far_c = 4 * cur + 3 - near_c;
         const float plane = __fmul_rn(diff, diff);
+        const float worst = KC > 0 ? bd[KA - 1] : bd[kk - 1];
         int64_t next;
         if (prev == par) {
             // first visit: the node's own point
             const float dd = dist2(q, p, k);
             const int32_t node = (int32_t)cur;
-            if (dd < bd[K - 1] || (dd == bd[K - 1] && node < bn[K - 1])) {
-                int j = K - 1;
-                while (j > 0 && (dd < bd[j - 1] || (dd == bd[j - 1] && node < bn[j - 1]))) {
+            if (KC > 0) {
+                if (knn_before(dd, node, bd[KA - 1], bn[KA - 1])) {
+                    // slot j takes the old j-1 if the new pair comes before
+                    // it, else the new pair if it comes before the old j
+#pragma unroll
+                    for (int j = KA - 1; j > 0; --j) {
+                        if (knn_before(dd, node, bd[j - 1], bn[j - 1])) {
+                            bd[j] = bd[j - 1];
+                            bn[j] = bn[j - 1];
+                        } else if (knn_before(dd, node, bd[j], bn[j])) {
+                            bd[j] = dd;
+                            bn[j] = node;
+                        }
+                    }
+                    if (knn_before(dd, node, bd[0], bn[0])) {
+                        bd[0] = dd;
+                        bn[0] = node;
+                    }
+                }
+            } else if (knn_before(dd, node, bd[kk - 1], bn[kk - 1])) {
+                int j = kk - 1;
+                while (j > 0 && knn_before(dd, node, bd[j - 1], bn[j - 1])) {
                     bd[j] = bd[j - 1];
                     bn[j] = bn[j - 1];
                     --j;
@@ -143,10 +175,11 @@ __global__ void __launch_bounds__(kQueryThreads) knn_kernel(const float *__restr
                 bd[j] = dd;
                 bn[j] = node;
             }
+            const float w2 = KC > 0 ? bd[KA - 1] : bd[kk - 1];
             if (near_c < N) next = near_c;
-            else next = (far_c < N && plane <= bd[K - 1]) ? far_c : par;
+            else next = (far_c < N && plane <= w2) ? far_c : par;
         } else if (prev == near_c) {
-            next = (far_c < N && plane <= bd[K - 1]) ? far_c : par;
+            next = (far_c < N && plane <= worst) ? far_c : par;
         } else {
             next = par;
         }
@@ -155,9 +188,11 @@ __global__ void __launch_bounds__(kQueryThreads) knn_kernel(const float *__restr
         cur = next;
     }
     if (it >= cap) set_status(status, KDT_EINTERNAL);
-    for (int j = 0; j < K; ++j) {
-        out_node[qi * K + j] = bn[j];
-        out_dist2[qi * K + j] = bd[j];
+#pragma unroll
+    for (int j = 0; j < KA; ++j) {
+        if (KC == 0 && j >= kk) break;
+        out_node[qi * kk + j] = bn[j];
+        out_dist2[qi * kk + j] = bd[j];
     }
 }
 
@@ -198,8 +233,22 @@ int enqueue_knn(const float *tree_pts, int64_t N, int k, const uint8_t *dims, co
     if (Q == 0) return KDT_OK;
     ProfScope ps(stream, "knn", 0.0);
     const unsigned blocks = (unsigned)((Q + kQueryThreads - 1) / kQueryThreads);
-    knn_kernel<<<blocks, kQueryThreads, 0, stream>>>(tree_pts, N, k, dims, queries, Q, K, out_node, out_dist2,
-                                                      status);
+    switch (K) {
+#define KDT_KNN_CASE(KK)                                                                                        \
+    case KK:                                                                                                    \
+        knn_kernel<KK><<<blocks, kQueryThreads, 0, stream>>>(tree_pts, N, k, dims, queries, Q, K, out_node,   \
+                                                             out_dist2, status);                               \
+        break;
+        KDT_KNN_CASE(1)
+        KDT_KNN_CASE(2)
+        KDT_KNN_CASE(4)
+        KDT_KNN_CASE(8)
+        KDT_KNN_CASE(16)
+#undef KDT_KNN_CASE
+        default:
+            knn_kernel<0><<<blocks, kQueryThreads, 0, stream>>>(tree_pts, N, k, dims, queries, Q, K, out_node,
+                                                                out_dist2, status);
+    }
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ECUDA;
 }
 
