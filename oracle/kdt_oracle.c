@@ -26,7 +26,7 @@
  *        neighbour problem statement (K nearest reference points of a query
  *        in Euclidean distance) -- for the query routines at the end.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - the super key is cyclic from the split dimension p: (x[p], x[p+1 mod k],
  *     ..., x[p-1 mod k]) and, when all coordinates are equal, the original
  *     input index breaks the tie; this makes the order strict and total, so
@@ -460,7 +460,7 @@ int kdo_node_dims(const float *tree_pts, int64_t N, int k, int mode, uint8_t *di
 /* ---- k nearest neighbours, by brute force ----------------------------------
  * "Bigger Buffer k-d Trees on Multi-Many-Core Systems", nearest-neighbour
  * problem statement: the K points of the reference set closest to a query in
- * Euclidean distance.  Readings (listed in the design doc): the distance is the
+ * Euclidean distance.  Readings where the page is silent: the distance is the
  * squared distance sum_{c=0..k-1} (q[c] - p[c])^2, accumulated left to right
  * in float32 with every operation rounded (no fused multiply-add); the
  * reference points are the tree's nodes; the result is the K smallest pairs
