@@ -11,7 +11,7 @@
 // In the paper every step sorts all points by (subtree tag, split key) and
 // then reads each point's new tag off its sorted position.  Only one fact of
 // that sort is used -- which side of rank ss(lChild(s)) a point falls on --
-// so this build replaces the sort by an exact rank select plus a partition,
+// so this builder replaces the sort by an exact rank select plus a partition,
 // which gives the same subtree sets and therefore the same tree.  The array
 // layout is the paper's: after level l the F(l+1) fixed nodes own positions
 // 0..F(l+1)-1 (their points go straight to the output), and live subtree s
