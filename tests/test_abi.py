@@ -73,3 +73,17 @@ def test_profile_switch_without_launches(lib):
     kdt.profile_reset()
     assert kdt.profile_read() == []
     kdt.profile_enable(False)
+
+
+def test_kernel_stat_struct_matches_the_header(lib):
+    """The ctypes mirror of kdt_kernel_stat has the header's fields, in order,
+    with the same widths (the binding reads the array the library fills)."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(kdt.__file__), os.pardir, "include", "kdtree_build.h")).read()
+    body = re.search(r"typedef struct \{([^}]*)\} kdt_kernel_stat;", hdr).group(1)
+    fields = re.findall(r"^\s*([A-Za-z_][A-Za-z_0-9 ]*?)\s*\*?\s*([A-Za-z_][A-Za-z_0-9]*);", body, re.M)
+    ctype_of = {"const char": ctypes.c_char_p, "int64_t": ctypes.c_int64, "double": ctypes.c_double}
+    want = [(name, ctype_of[t.strip()]) for t, name in fields]
+    assert kdt._KernelStat._fields_ == want
+    assert ctypes.sizeof(kdt._KernelStat) == 40
