@@ -33,14 +33,18 @@ constexpr int kInitThreads = 256;
 
 constexpr int kInitPPT = 4;  // points per thread per iteration
 
+// KM: compile-time bound on k (4, 8, 16 or 32), so that the per-dimension
+// minima and maxima stay in registers without reserving 2 * KDT_MAX_K of them
+// for small k.
+template <int KM>
 __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restrict__ pts, int64_t N,
                                                             int k, int64_t ld, uint32_t *__restrict__ keys,
                                                             uint32_t *__restrict__ idx,
                                                             uint32_t *__restrict__ bbox,
                                                             int *__restrict__ status) {
-    uint32_t mn[kMaxK], mx[kMaxK];
+    uint32_t mn[KM], mx[KM];
 #pragma unroll
-    for (int c = 0; c < kMaxK; ++c) {
+    for (int c = 0; c < KM; ++c) {
         mn[c] = 0xffffffffu;
         mx[c] = 0u;
     }
@@ -49,7 +53,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
     for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < N; i0 += nt * kInitPPT) {
         // one dimension at a time: the kInitPPT loads go out before the stores
 #pragma unroll
-        for (int c = 0; c < kMaxK; ++c) {
+        for (int c = 0; c < KM; ++c) {
             if (c < k) {
                 float f[kInitPPT];
 #pragma unroll
@@ -80,7 +84,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
 #pragma unroll
-    for (int c = 0; c < kMaxK; ++c) {
+    for (int c = 0; c < KM; ++c) {
         if (c < k) {
             const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
             const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
@@ -199,9 +203,19 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         ProfScope ps(stream, "init", 0.0);
         // the input-index column starts as the identity: written only if the
         // finisher takes the root subtree (global levels use the position)
-        init_kernel<<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0],
-                                                                   p.finish_level == 0 ? b.idx[0] : nullptr, b.bbox,
-                                                                   b.status);
+        uint32_t *idx0 = p.finish_level == 0 ? b.idx[0] : nullptr;
+        if (k <= 4)
+            init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0, b.bbox,
+                                                                          b.status);
+        else if (k <= 8)
+            init_kernel<8><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0, b.bbox,
+                                                                          b.status);
+        else if (k <= 16)
+            init_kernel<16><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0,
+                                                                           b.bbox, b.status);
+        else
+            init_kernel<32><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0,
+                                                                           b.bbox, b.status);
         KDT_LAUNCH_CHECK();
     }
     {

@@ -190,7 +190,7 @@ __device__ void group_split_node(const G &grp, const FinArgs &a, const FinSmem &
         return;
     }
     const uint32_t tid = grp.tid(), nt = grp.size();
-    if (tid <= (uint32_t)k) medw[tid] = acc((int)tid, st.med_q);
+    for (uint32_t i = tid; i <= (uint32_t)k; i += nt) medw[i] = acc((int)i, st.med_q);  // k + 1 words, k <= 32
     if (tid < 2) cur2[tid] = 0u;
     grp.sync();
     const uint32_t lane = lane_id(), lt = (1u << lane) - 1u;

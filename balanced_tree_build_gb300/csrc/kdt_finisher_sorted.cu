@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         if (tid == 0) sm.ldim[0] = (uint8_t)sf_widest_dim(a, sm, s0, 0, 0);
         __syncthreads();
     }
-    const uint32_t allk = (1u << k) - 1u;  // k <= KDT_MAX_K < 32
+    const uint32_t allk = k >= 32 ? 0xffffffffu : (1u << k) - 1u;  // k <= KDT_MAX_K = 32
     int dl0 = rr ? a.l0 % k : 0;           // round-robin split coordinate of level l
     int par = 0;
     for (int l = 0; l <= last; ++l, dl0 = dl0 + 1 == k ? 0 : dl0 + 1) {
@@ -386,8 +386,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         if (rr) {
             const int m = last - l;
             if (m < k - 1) {
-                const uint32_t run = ((1u << m) - 1u) << (dl0 + 1);  // bits dl0+1 .. dl0+m, unwrapped
-                mv = (run | (run >> k)) & allk;
+                // bits dl0+1 .. dl0+m, unwrapped (at most bit 62 for k = 32), then folded mod k
+                const uint64_t run = ((1ull << m) - 1ull) << (dl0 + 1);
+                mv = (uint32_t)((run | (run >> k)) & allk);
             }
             mv &= ~(1u << dl0);
             if (mv == 0u) break;  // k >= 2: only for l >= h-2; k == 1: never moves

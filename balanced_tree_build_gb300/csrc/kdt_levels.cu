@@ -428,7 +428,7 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    if (tid <= (uint32_t)k) medw[tid] = acc((int)tid, st.med_q);
+    for (uint32_t i = tid; i <= (uint32_t)k; i += nt) medw[i] = acc((int)i, st.med_q);  // k + 1 words, k <= 32
     if (tid < 2) cur2[tid] = 0u;
     __syncthreads();
     Bucketer bkc;

@@ -90,7 +90,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "50"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -211,9 +211,11 @@ def cpu_baseline(workload, budget_s: float = 12.0) -> dict:
         o.build_tree(pts, workload.mode)
         dt = time.perf_counter() - t0
     return {"value": sample_n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{sample_n} points drawn from the {workload.name} distribution "
-                      f"(k={workload.k}, mode={workload.mode}), one full build, {reps} run, "
-                      f"single-threaded C oracle"}
+            "sample_points": sample_n, "workload_points": workload.n,
+            "sample": f"a SAMPLE of {sample_n} points (not the workload's {workload.n}) drawn from the "
+                      f"{workload.name} distribution (k={workload.k}, mode={workload.mode}), one full build, "
+                      f"{reps} run, single-threaded C oracle; the oracle sorts each subtree "
+                      f"(O(N log^2 N)), so its rate at the full size is lower"}
 
 
 def run_reference(args, workload):
@@ -328,6 +330,69 @@ def knn_extra(kdt, tree_pts, workload, stream, n_queries: int = 1 << 20, K: int 
             "tree_points": n, "api": "kdt_knn (one thread per query, stack-free descent and backtrack)"}
 
 
+def time_steps(step, stream, n_steps: int) -> float:
+    """Milliseconds for n_steps calls of step(), CUDA events on `stream`
+    with a device synchronisation on both sides."""
+    import torch
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n_steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
+
+
+def workload_rows(kdt, dev, stream, peak, names, steps: int, oracle_full: bool) -> list[dict]:
+    """The smaller workloads, each timed like the headline one (device-resident
+    points, caller workspace, CUDA events over `steps` builds after 3 warm-up
+    builds), checked by the GPU verifier and, unless disabled, element by
+    element against the CPU oracle run on the same full-size input (its
+    single-threaded build time is reported beside the GPU's)."""
+    import numpy as np
+    import torch
+    from balanced_tree_build_gb300.inputs import WORKLOADS
+    rows = []
+    for name in names:
+        w = WORKLOADS[name]
+        host = w.points()
+        pts = torch.from_numpy(host).to(dev)
+        perm = torch.empty(w.n, dtype=torch.int32, device=dev)
+        ws = kdt.alloc_workspace(w.n, w.k, w.mode, device=dev)
+
+        def step():
+            kdt.build_tree(pts, w.mode, out=perm, workspace=ws, stream=stream)
+
+        for _ in range(3):
+            step()
+        ms = time_steps(step, stream, steps) / steps
+        rc = kdt.status(stream)
+        if rc != 0:
+            raise SystemExit(f"{name}: device status {rc}")
+        if not kdt.verify_tree(pts, perm, w.mode, stream=stream):
+            raise SystemExit(f"{name}: the GPU verifier rejected the tree")
+        balg = b_alg(w.n)
+        gbs = balg / (ms / 1e3) / 1e9
+        row = {"workload": name, "N": w.n, "k": w.k, "split_mode": "round_robin" if w.mode == 0 else "widest",
+               "ms_per_build": ms, "points_per_s": w.n / (ms / 1e3), "B_alg_bytes": balg,
+               "frac_of_measured": gbs / peak, "frac_of_nominal_8TBps": gbs / NOMINAL_HBM_GBS,
+               "builds_timed": steps, "verified": "gpu verifier"}
+        if oracle_full:
+            import oracle
+            t0 = time.perf_counter()
+            want = oracle.get().build_tree(host, w.mode)
+            row["oracle_s"] = time.perf_counter() - t0
+            row["oracle_points_per_s"] = w.n / row["oracle_s"]
+            if not np.array_equal(perm.cpu().numpy(), want):
+                raise SystemExit(f"{name}: the GPU tree differs from the oracle's")
+            row["verified"] = "gpu verifier + bit-exact equal to the full-size oracle build"
+        rows.append(row)
+        del pts, perm, ws
+    return rows
+
+
 def run_ours(args, workload):
     import torch
     import balanced_tree_build_gb300 as kdt
@@ -354,35 +419,39 @@ def run_ours(args, workload):
     if rc != 0:
         raise SystemExit(f"device status after warm-up: {rc}")
 
+    # timed region: the library's per-kernel timing is off here
+    kdt.profile_enable(False)
     sampler = ClockSampler(gpu_identifier(local))
-    kdt.profile_reset()
-    kdt.profile_enable(True)
     barrier(active)
     torch.cuda.synchronize(dev)
     sampler.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms = time_steps(step, stream, args.steps)
     barrier(active)
     clocks = sampler.stop()
-    kdt.profile_enable(False)
-    stats = kdt.profile_read()
-    ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, active, dev if active else None)
     rc = kdt.status(stream)
     if rc != 0:
         raise SystemExit(f"device status after timed steps: {rc}")
+    # the last timed build's output, checked on the GPU (every node against
+    # every ancestor, plus the permutation check)
+    if not kdt.verify_tree(pts, perm, workload.mode, stream=stream):
+        raise SystemExit("the GPU verifier rejected the benchmarked tree")
 
     total_points = float(n) * args.steps * world
     value = total_points / (ms_max / 1e3)
     ms_step = ms_max / args.steps
 
+    # separate profiled pass: per-kernel CUDA events on the build's stream
+    prof_steps = max(1, min(args.steps, 5))
+    kdt.profile_reset()
+    kdt.profile_enable(True)
+    prof_ms = time_steps(step, stream, prof_steps)
+    kdt.profile_enable(False)
+    stats = kdt.profile_read()
+    kdt.profile_reset()
+
     peak, peak_src = measured_peaks()
-    launches = sum(s["kernels"] for s in stats)  # kernel launches inside the timed scopes
+    launches_per_build = sum(s["kernels"] for s in stats) / prof_steps
     dom = max(stats, key=lambda s: s["total_ms"]) if stats else None
     roofline = None
     if dom:
@@ -392,7 +461,9 @@ def run_ours(args, workload):
         traffic = recorded_traffic(dom["name"]) if workload.name == "uniform_100m" else None
         roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                    "traffic": traffic, "avg_launch_ms": avg_ms, "alg_bytes_per_launch": avg_bytes}
+                    "traffic": traffic, "avg_launch_ms": avg_ms, "alg_bytes_per_launch": avg_bytes,
+                    "timing": f"CUDA events around each launch on the build's stream, in a separate "
+                              f"profiled pass of {prof_steps} builds after the timed region"}
     balg = b_alg(n)
     build_gbs = balg / (ms_step / 1e3) / 1e9
     build_roof = {"B_alg_bytes": balg, "achieved_GBps": build_gbs, "frac_of_measured": build_gbs / peak,
@@ -412,9 +483,20 @@ def run_ours(args, workload):
             kdt.build_tree_host(pin_pts, workload.mode, out=pin_out, workspace=hws, stream=stream)
         dt = time.perf_counter() - t0
         dt = max_over_ranks(dt, active, dev if active else None)
+        if not torch.equal(pin_out, perm.cpu()):
+            raise SystemExit("the host-buffer build differs from the device build")
+        # the link on its own, for context: one pinned H2D copy of the points
+        # and one D2H copy of the permutation (CUDA events)
+        tmp = torch.empty_like(pts)
+        h2d_ms = time_steps(lambda: tmp.copy_(pin_pts, non_blocking=True), stream, 3) / 3
+        d2h_ms = time_steps(lambda: pin_out.copy_(perm, non_blocking=True), stream, 3) / 3
+        del tmp
         e2e = {"value": float(n) * e_steps * world / dt, "unit": UNIT,
                "h2d_bytes_per_step": int(n * k * 4), "d2h_bytes_per_step": int(n * 4),
-               "steps": e_steps, "api": "kdt_build_host (pinned host buffers)"}
+               "steps": e_steps, "ms_per_step": dt * 1e3 / e_steps,
+               "api": "kdt_build_host (pinned host buffers)",
+               "link_alone": {"h2d_ms": h2d_ms, "h2d_GBps": n * k * 4 / (h2d_ms / 1e3) / 1e9,
+                              "d2h_ms": d2h_ms, "d2h_GBps": n * 4 / (d2h_ms / 1e3) / 1e9}}
         del hws
 
     extras = None
@@ -422,6 +504,13 @@ def run_ours(args, workload):
         lo, tree_pts = level_order_extra(kdt, pts, perm, ws, workload, stream, peak)
         extras = {"level_order_points": lo, "knn": knn_extra(kdt, tree_pts, workload, stream)}
         del tree_pts
+    if not args.no_workloads and rank == 0:
+        del ws
+        torch.cuda.empty_cache()
+        extras = extras or {}
+        extras["workloads"] = workload_rows(kdt, dev, stream, peak,
+                                            ["uniform_1k", "uniform_pm1_1m", "mixture_dup_10m", "quant1024_k8_4m"],
+                                            10, not args.no_oracle_full)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -433,8 +522,9 @@ def run_ours(args, workload):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(workload, extra={"parallelism": f"replicas x{world}"}),
-            "roofline": roofline, "build_roofline": build_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "kernels": stats, "clocks": clocks, "extras": extras,
+            "verified": True, "roofline": roofline, "build_roofline": build_roof, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": int(round(launches_per_build * args.steps)),
+            "kernels": stats, "profiled_ms_per_step": prof_ms / prof_steps, "clocks": clocks, "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if active:
@@ -452,8 +542,12 @@ def main(argv=None):
     ap.add_argument("--workload", default="uniform_100m")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the level-order points timing")
-    ap.add_argument("--ref-sample", type=int, default=1 << 18,
+    ap.add_argument("--no-extras", action="store_true", help="skip the level-order points and kNN timings")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the rows for the four smaller workloads")
+    ap.add_argument("--no-oracle-full", action="store_true",
+                    help="skip the full-size oracle builds of the smaller workloads")
+    ap.add_argument("--ref-sample", type=int, default=1 << 20,
                     help="points per step for --impl reference")
     ap.add_argument("--n", type=int, default=None,
                     help="build a sample of this many points of the workload's distribution "

@@ -70,7 +70,7 @@ extern "C" {
 #define KDT_SPLIT_ROUND_ROBIN 0
 #define KDT_SPLIT_WIDEST 1
 
-#define KDT_MAX_K 16
+#define KDT_MAX_K 32
 
 /* Bytes of device scratch that a build of (N, k, split_mode) needs.
  * Host-only; returns KDT_EINVAL for arguments kdt_build would reject. */

@@ -26,7 +26,7 @@ def gpu_tree(pts, mode):
 
 
 @pytest.mark.parametrize("dist,k", [("uniform01", 3), ("gaussian", 2), ("quant1024", 8), ("dup_heavy", 5),
-                                    ("signed_zero", 3), ("all_equal", 4)])
+                                    ("signed_zero", 3), ("all_equal", 4), ("uniform01", 32)])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_node_dims_match_oracle(o, dist, k, mode):
     pts = make_points(dist, 3001, k, seed=k + 17)
@@ -52,7 +52,8 @@ def check_knn(o, tree_np, queries_np, K, mode, tree=None, dims=None):
 
 
 @pytest.mark.parametrize("dist,k", [("uniform01", 3), ("gaussian", 3), ("dup_heavy", 2), ("signed_zero", 3),
-                                    ("all_equal", 3), ("int_grid", 4), ("quant1024", 8)])
+                                    ("all_equal", 3), ("int_grid", 4), ("quant1024", 8),
+                                    ("gaussian", 32)])
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("K", [1, 4, 16])
 def test_knn_matches_oracle(o, dist, k, mode, K):

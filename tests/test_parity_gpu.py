@@ -78,6 +78,17 @@ def test_round_robin_many_dims_multi_level(o, n, k, dist):
     assert_parity(o, make_points(dist, n, k, seed=n + 31 * k), 0)
 
 
+@pytest.mark.parametrize("k", [17, 24, 31, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("dist", ["uniform01", "dup_heavy", "quant1024"])
+def test_many_dimensions_up_to_the_limit(o, k, mode, dist):
+    """k up to KDT_MAX_K = 32: small tiles (the finisher's shared memory holds
+    k key columns), every coordinate split on, and round-robin masks that wrap
+    past bit 31."""
+    for n in (1, 333, 9_001, 70_003):
+        assert_parity(o, make_points(dist, n, k, seed=n + 97 * k + mode), mode)
+
+
 @pytest.mark.parametrize("dist", ["all_equal", "dup_heavy", "quant1024", "signed_zero"])
 def test_heavy_ties_multi_level(o, dist):
     assert_parity(o, make_points(dist, 150_000, 3, seed=5), 0)

@@ -23,7 +23,7 @@ def bits(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 
 
-@pytest.mark.parametrize("k", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 5, 8, 16, 32])
 @pytest.mark.parametrize("n", [1, 2, 7, 1000, 4097])
 def test_gather_matches_oracle(o, k, n):
     pts = make_points("signed_zero" if k % 2 else "gaussian", n, k, seed=n + k)
