@@ -210,12 +210,16 @@ __device__ __forceinline__ uint32_t ids_at(const uint4 &v, int e) {
     return (e & 1) ? (wv >> 16) : (wv & 0xffffu);
 }
 
-template <int NT, bool RR>
+// RR: round-robin split rule; K3: round-robin with k = 3 (the levels move
+// each coordinate array once every three levels).
+template <int NT, bool RR, bool K3>
 __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __grid_constant__ SfArgs a) {
     constexpr int NW = NT / 32, E = kSfPPT;
+    static_assert(!K3 || RR, "the k = 3 schedule is a round-robin one");
     extern __shared__ __align__(16) unsigned char sf_smem[];
     __shared__ uint32_t red[64];
     __shared__ uint32_t wagg[2][NW];  // [round parity][warp]: segmented warp sums
+    __shared__ uint64_t wagg64[NW];   // k = 3 schedule: segmented warp sums of the 4-field scan
     __shared__ int stop;
     const uint32_t tid = threadIdx.x;
     const uint32_t w = tid >> 5, lane = tid & 31u;
@@ -374,138 +378,255 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         if (tid == 0) sm.ldim[0] = (uint8_t)sf_widest_dim(a, sm, s0, 0, 0);
         __syncthreads();
     }
-    const uint32_t allk = k >= 32 ? 0xffffffffu : (1u << k) - 1u;  // k <= KDT_MAX_K = 32
-    int dl0 = rr ? a.l0 % k : 0;           // round-robin split coordinate of level l
-    int par = 0;
-    for (int l = 0; l <= last; ++l, dl0 = dl0 + 1 == k ? 0 : dl0 + 1) {
-        // arrays to partition on this level: round-robin -- those that some
-        // level in (l, last] splits on (the last - l coordinates after dl0,
-        // cyclically), except this level's own; widest -- all (a node's own
-        // split array is skipped per point)
-        uint32_t mv = allk;
-        if (rr) {
-            const int m = last - l;
-            if (m < k - 1) {
-                // bits dl0+1 .. dl0+m, unwrapped (at most bit 62 for k = 32), then folded mod k
-                const uint64_t run = ((1ull << m) - 1ull) << (dl0 + 1);
-                mv = (uint32_t)((run | (run >> k)) & allk);
-            }
-            mv &= ~(1u << dl0);
-            if (mv == 0u) break;  // k >= 2: only for l >= h-2; k == 1: never moves
-        }
-        // this level's node ranges: lo | pos << 16 per node
-        for (uint32_t i = tid; i < (1u << l); i += NT) sm.ntab[i] = io_lo(i, l, h, Mt) | (io_pos(i, l, h, Mt) << 16);
-        // live / head masks: a node range starts at p if p is live and p-1
-        // is not (p-1 holds a fixed ancestor, or p == 0)
-        uint32_t live = 0u, head = 0u;
-        if (wact) {
-            bool pl = (gprev << (l + 1)) != 0u;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const bool lv = (g[e] << (l + 1)) != 0u;
-                live |= (uint32_t)lv << e;
-                head |= (uint32_t)(lv && !pl) << e;
-                pl = lv;
-            }
-            if (p0 == 0u) head |= live & 1u;
-            // phase A: side increments from the split arrays
-            if (rr) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(sm.ids + dl0 * T + p0);
+    if constexpr (K3) {
+        // Round-robin, k = 3: each coordinate array is moved once every three
+        // levels instead of twice.  On level l the split array d_l is in order
+        // for the nodes of level l.  Array d_{l+1} was last in order for the
+        // nodes of level l-1 (it was the split array of level l-2); here it
+        // absorbs the splits of levels l-1 and l in one pass: each point of a
+        // level-(l-1) node w goes to one of w's four grandchildren, or is the
+        // split point of w or of one of w's children (fixed at its position).
+        // Level 0 moves d_1 by the root's split alone.  The scan carries the
+        // four grandchildren's first positions (16-bit fields of a 64-bit
+        // word, set at the first position of w's range), so a point's
+        // destination is one field of its running value.
+        constexpr uint64_t kHead64 = 1ull << 63;
+        uint32_t *side32 = sm.side;                                 // [T]: two 16-bit sides, by level parity
+        uint16_t *side16 = reinterpret_cast<uint16_t *>(sm.side);
+        uint16_t *ptab0 = reinterpret_cast<uint16_t *>(sm.ntab);   // [T/2] in-order position of each node of a level
+        uint16_t *ptab1 = ptab0 + T / 2;
+        int dl = a.l0 % 3;
+        for (int l = 0; l < last; ++l, dl = dl == 2 ? 0 : dl + 1) {
+            const uint32_t q = (uint32_t)l & 1u;
+            uint16_t *pt_l = q ? ptab1 : ptab0;
+            const uint16_t *pt_p = q ? ptab0 : ptab1;  // level l - 1
+            for (uint32_t i = tid; i < (1u << l); i += NT) pt_l[i] = (uint16_t)io_pos(i, l, h, Mt);
+            // A: side of every point of a level-l node, from d_l: 0 left,
+            //    1 right, 0x8000 | position for the node's split point
+            if (wact) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(sm.ids + dl * T + p0);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    if (!((live >> e) & 1u)) continue;
                     const uint32_t t = g[e] << (l + 1);
-                    sm.side[ids_at(v, e) & tmask] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    if (!((live >> e) & 1u)) continue;
-                    const uint32_t t = g[e] << (l + 1);
-                    const uint32_t ga = g[e] >> (31 - l);
-                    const int d = sm.ldim[ga ^ (1u << l)];
-                    const uint32_t id = sm.ids[d * T + p0 + e] & tmask;
-                    sm.side[id] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
-                    if (t == 0x80000000u) {
-                        const uint32_t ib = id < n ? id : 0u;  // a permutation of [0, n) unless corrupt
-                        sm.sval[ga - 1u] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + ib));
-                        sm.sdim[ga - 1u] = (uint8_t)d;
-                    }
+                    if (t == 0u) continue;
+                    const uint32_t id = ids_at(v, e) & tmask;
+                    side16[2u * id + q] = (uint16_t)(t == 0x80000000u ? (0x8000u | (p0 + (uint32_t)e)) : (t >> 31));
                 }
             }
-        }
-        __syncthreads();
-        // phases B and D, one array at a time (B of the next array may run
-        // while slower warps finish D of this one: different arrays, and the
-        // warp sums alternate between two buffers)
-        uint32_t rest = mv;
-        while (rest != 0u) {
-            const int c = __ffs((int)rest) - 1;
-            rest &= rest - 1u;
+            __syncthreads();
+            const int c = dl == 2 ? 0 : dl + 1;  // d_{l+1}
+            // B: live positions of level l-1 (level 0: the whole tile), running
+            //    value before each held point, warp scan
             uint4 iv = make_uint4(0u, 0u, 0u, 0u);
-            uint32_t X[E], mask = 0u, exw = 0u;
-            // B: running left | right << 16 counts before each held point,
-            // from its range start (kSegHead set) or from p0; warp scan
+            uint64_t X[E];
+            uint32_t mask = 0u;
+            uint64_t exw = 0ull;
             if (wact) {
                 iv = *reinterpret_cast<const uint4 *>(sm.ids + c * T + p0);
-                mask = live;
-                if (!rr) {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        if (!((live >> e) & 1u)) continue;
-                        if (sm.ldim[(g[e] >> (31 - l)) ^ (1u << l)] == c) mask &= ~(1u << e);  // own split array
-                    }
-                }
-                uint32_t run = 0u;
+                bool pl = (gprev << l) != 0u;
+                uint64_t run = 0ull;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    if ((head >> e) & 1u) run = kSegHead;
+                    const bool lv = (g[e] << l) != 0u;
+                    if (lv && !pl) {  // first position of a level-(l-1) node w
+                        uint64_t base = (uint64_t)(p0 + (uint32_t)e);
+                        if (l == 0) {
+                            base |= (uint64_t)(pt_l[0] + 1u) << 16;
+                        } else {
+                            const uint32_t wi = (g[e] >> (32 - l)) ^ (1u << (l - 1));
+                            base |= ((uint64_t)(pt_l[2u * wi] + 1u) << 16) | ((uint64_t)(pt_p[wi] + 1u) << 32) |
+                                    ((uint64_t)(pt_l[2u * wi + 1u] + 1u) << 48);
+                        }
+                        run = kHead64 | base;
+                    }
+                    pl = lv;
                     X[e] = run;
-                    if ((mask >> e) & 1u) run += sm.side[ids_at(iv, e) & tmask];
+                    if (lv) {
+                        mask |= 1u << e;
+                        const uint32_t sw = side32[ids_at(iv, e) & tmask];
+                        const uint32_t s1 = l == 0 ? 0u : (sw >> (16u * (q ^ 1u))) & 0xffffu;
+                        const uint32_t s2 = (sw >> (16u * q)) & 0xffffu;
+                        if (!((s1 | s2) & 0x8000u)) run += 1ull << (16u * (2u * s1 + s2));
+                    }
                 }
-                uint32_t x = run;
+                uint64_t x = run;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= (uint32_t)o) x = seg_combine(y, x);
+                    const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= (uint32_t)o) x = (x & kHead64) ? x : y + x;
                 }
-                if (lane == 31u) wagg[par][w] = x;
-                const uint32_t ex = __shfl_up_sync(0xffffffffu, x, 1);
-                exw = lane == 0u ? 0u : ex;
+                if (lane == 31u) wagg64[w] = x;
+                const uint64_t ex = __shfl_up_sync(0xffffffffu, x, 1);
+                exw = lane == 0u ? 0ull : ex;
             }
             __syncthreads();
             // D: carry from the warps before, destinations, in-place stores
             if (wact) {
-                uint32_t v = lane < (uint32_t)NW ? wagg[par][lane] : 0u;
+                uint64_t v = lane < (uint32_t)NW ? wagg64[lane] : 0ull;
 #pragma unroll
                 for (int o = 1; o < NW; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= (uint32_t)o) v = seg_combine(y, v);
+                    const uint64_t y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= (uint32_t)o) v = (v & kHead64) ? v : y + v;
                 }
-                const uint32_t cw = __shfl_sync(0xffffffffu, v, (w + 31u) & 31u);
-                const uint32_t lb = (exw & kSegHead) ? (exw & ~kSegHead) : (w > 0u ? (cw & ~kSegHead) : 0u) + exw;
+                const uint64_t cw = __shfl_sync(0xffffffffu, v, (w + 31u) & 31u);
+                const uint64_t lb =
+                    (exw & kHead64) ? (exw & ~kHead64) : (w > 0u ? (cw & ~kHead64) : 0ull) + exw;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     if (!((mask >> e) & 1u)) continue;
                     const uint32_t id = ids_at(iv, e);
-                    const uint32_t inc = sm.side[id & tmask];
-                    const uint32_t val = (X[e] & kSegHead) ? (X[e] & ~kSegHead) : lb + X[e];
-                    const uint32_t nt = sm.ntab[(g[e] >> (31 - l)) ^ (1u << l)];
-                    const uint32_t pos = nt >> 16;
-                    const uint32_t dst = inc == 1u ? (nt & 0xffffu) + (val & 0xffffu)
-                                                   : (inc == 0u ? pos : pos + 1u + (val >> 16));
+                    const uint32_t sw = side32[id & tmask];
+                    const uint32_t s1 = l == 0 ? 0u : (sw >> (16u * (q ^ 1u))) & 0xffffu;
+                    const uint32_t s2 = (sw >> (16u * q)) & 0xffffu;
+                    uint32_t dst;
+                    if (s1 & 0x8000u) {
+                        dst = s1 & 0x1fffu;
+                    } else if (s2 & 0x8000u) {
+                        dst = s2 & 0x1fffu;
+                    } else {
+                        const uint64_t val = (X[e] & kHead64) ? (X[e] & ~kHead64) : lb + X[e];
+                        dst = (uint32_t)(val >> (16u * (2u * s1 + s2))) & 0x1fffu;
+                    }
                     if (dst < n) sm.ids[c * T + dst] = (uint16_t)id;
                     else set_status(a.status, KDT_EINTERNAL);
                 }
             }
-            par ^= 1;
+            __syncthreads();
         }
-        // widest: split dimensions of the next level's nodes (their
-        // ancestors' split values were recorded in phase A)
-        if (!rr && l + 1 <= last) {
-            for (uint32_t i = tid; i < (1u << (l + 1)); i += NT) sm.ldim[i] = (uint8_t)sf_widest_dim(a, sm, s0, l + 1, (int32_t)i);
+    } else {
+        const uint32_t allk = k >= 32 ? 0xffffffffu : (1u << k) - 1u;  // k <= KDT_MAX_K = 32
+        int dl0 = rr ? a.l0 % k : 0;           // round-robin split coordinate of level l
+        int par = 0;
+        for (int l = 0; l <= last; ++l, dl0 = dl0 + 1 == k ? 0 : dl0 + 1) {
+            // arrays to partition on this level: round-robin -- those that some
+            // level in (l, last] splits on (the last - l coordinates after dl0,
+            // cyclically), except this level's own; widest -- all (a node's own
+            // split array is skipped per point)
+            uint32_t mv = allk;
+            if (rr) {
+                const int m = last - l;
+                if (m < k - 1) {
+                    // bits dl0+1 .. dl0+m, unwrapped (at most bit 62 for k = 32), then folded mod k
+                    const uint64_t run = ((1ull << m) - 1ull) << (dl0 + 1);
+                    mv = (uint32_t)((run | (run >> k)) & allk);
+                }
+                mv &= ~(1u << dl0);
+                if (mv == 0u) break;  // k >= 2: only for l >= h-2; k == 1: never moves
+            }
+            // this level's node ranges: lo | pos << 16 per node
+            for (uint32_t i = tid; i < (1u << l); i += NT) sm.ntab[i] = io_lo(i, l, h, Mt) | (io_pos(i, l, h, Mt) << 16);
+            // live / head masks: a node range starts at p if p is live and p-1
+            // is not (p-1 holds a fixed ancestor, or p == 0)
+            uint32_t live = 0u, head = 0u;
+            if (wact) {
+                bool pl = (gprev << (l + 1)) != 0u;
+    #pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const bool lv = (g[e] << (l + 1)) != 0u;
+                    live |= (uint32_t)lv << e;
+                    head |= (uint32_t)(lv && !pl) << e;
+                    pl = lv;
+                }
+                if (p0 == 0u) head |= live & 1u;
+                // phase A: side increments from the split arrays
+                if (rr) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sm.ids + dl0 * T + p0);
+    #pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if (!((live >> e) & 1u)) continue;
+                        const uint32_t t = g[e] << (l + 1);
+                        sm.side[ids_at(v, e) & tmask] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
+                    }
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if (!((live >> e) & 1u)) continue;
+                        const uint32_t t = g[e] << (l + 1);
+                        const uint32_t ga = g[e] >> (31 - l);
+                        const int d = sm.ldim[ga ^ (1u << l)];
+                        const uint32_t id = sm.ids[d * T + p0 + e] & tmask;
+                        sm.side[id] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
+                        if (t == 0x80000000u) {
+                            const uint32_t ib = id < n ? id : 0u;  // a permutation of [0, n) unless corrupt
+                            sm.sval[ga - 1u] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + ib));
+                            sm.sdim[ga - 1u] = (uint8_t)d;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            // phases B and D, one array at a time (B of the next array may run
+            // while slower warps finish D of this one: different arrays, and the
+            // warp sums alternate between two buffers)
+            uint32_t rest = mv;
+            while (rest != 0u) {
+                const int c = __ffs((int)rest) - 1;
+                rest &= rest - 1u;
+                uint4 iv = make_uint4(0u, 0u, 0u, 0u);
+                uint32_t X[E], mask = 0u, exw = 0u;
+                // B: running left | right << 16 counts before each held point,
+                // from its range start (kSegHead set) or from p0; warp scan
+                if (wact) {
+                    iv = *reinterpret_cast<const uint4 *>(sm.ids + c * T + p0);
+                    mask = live;
+                    if (!rr) {
+    #pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            if (!((live >> e) & 1u)) continue;
+                            if (sm.ldim[(g[e] >> (31 - l)) ^ (1u << l)] == c) mask &= ~(1u << e);  // own split array
+                        }
+                    }
+                    uint32_t run = 0u;
+    #pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if ((head >> e) & 1u) run = kSegHead;
+                        X[e] = run;
+                        if ((mask >> e) & 1u) run += sm.side[ids_at(iv, e) & tmask];
+                    }
+                    uint32_t x = run;
+    #pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= (uint32_t)o) x = seg_combine(y, x);
+                    }
+                    if (lane == 31u) wagg[par][w] = x;
+                    const uint32_t ex = __shfl_up_sync(0xffffffffu, x, 1);
+                    exw = lane == 0u ? 0u : ex;
+                }
+                __syncthreads();
+                // D: carry from the warps before, destinations, in-place stores
+                if (wact) {
+                    uint32_t v = lane < (uint32_t)NW ? wagg[par][lane] : 0u;
+    #pragma unroll
+                    for (int o = 1; o < NW; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= (uint32_t)o) v = seg_combine(y, v);
+                    }
+                    const uint32_t cw = __shfl_sync(0xffffffffu, v, (w + 31u) & 31u);
+                    const uint32_t lb = (exw & kSegHead) ? (exw & ~kSegHead) : (w > 0u ? (cw & ~kSegHead) : 0u) + exw;
+    #pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        if (!((mask >> e) & 1u)) continue;
+                        const uint32_t id = ids_at(iv, e);
+                        const uint32_t inc = sm.side[id & tmask];
+                        const uint32_t val = (X[e] & kSegHead) ? (X[e] & ~kSegHead) : lb + X[e];
+                        const uint32_t nt = sm.ntab[(g[e] >> (31 - l)) ^ (1u << l)];
+                        const uint32_t pos = nt >> 16;
+                        const uint32_t dst = inc == 1u ? (nt & 0xffffu) + (val & 0xffffu)
+                                                       : (inc == 0u ? pos : pos + 1u + (val >> 16));
+                        if (dst < n) sm.ids[c * T + dst] = (uint16_t)id;
+                        else set_status(a.status, KDT_EINTERNAL);
+                    }
+                }
+                par ^= 1;
+            }
+            // widest: split dimensions of the next level's nodes (their
+            // ancestors' split values were recorded in phase A)
+            if (!rr && l + 1 <= last) {
+                for (uint32_t i = tid; i < (1u << (l + 1)); i += NT) sm.ldim[i] = (uint8_t)sf_widest_dim(a, sm, s0, l + 1, (int32_t)i);
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 
     // 4. output: node u of the tile (level lv, index i) reads its point at
@@ -548,19 +669,20 @@ int pick_tile(int k, int mode, TilePlan *tp) {
     return -1;
 }
 
-template <int NT, bool RR>
+template <int NT, bool RR, bool K3>
 static int launch_sorted_mode(const SfArgs &a, int64_t ntiles, size_t smem, cudaStream_t stream) {
-    if (cudaFuncSetAttribute(sorted_finisher_kernel<NT, RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sorted_finisher_kernel<NT, RR, K3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return KDT_ECUDA;
-    sorted_finisher_kernel<NT, RR><<<(unsigned)ntiles, NT, smem, stream>>>(a);
+    sorted_finisher_kernel<NT, RR, K3><<<(unsigned)ntiles, NT, smem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ECUDA;
 }
 
 template <int NT>
 static int launch_sorted(const SfArgs &a, int64_t ntiles, size_t smem, cudaStream_t stream) {
-    return a.mode == KDT_SPLIT_ROUND_ROBIN ? launch_sorted_mode<NT, true>(a, ntiles, smem, stream)
-                                           : launch_sorted_mode<NT, false>(a, ntiles, smem, stream);
+    if (a.mode != KDT_SPLIT_ROUND_ROBIN) return launch_sorted_mode<NT, false, false>(a, ntiles, smem, stream);
+    return a.k == 3 ? launch_sorted_mode<NT, true, true>(a, ntiles, smem, stream)
+                    : launch_sorted_mode<NT, true, false>(a, ntiles, smem, stream);
 }
 
 int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream) {
