@@ -72,12 +72,13 @@ static size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Dynamic shared memory of one CTA: reference arrays [k][T] u16, keys [k][T]
 // u32 (after the sort: the partition increment of each point), input indices
-// [T], nb >= T 16-bit bucket counters (after the sort: the node ranges of a
-// level), a [T] u16 bucket staging array (after the sort, in widest mode: the
-// split dimension of each node of a level), and in widest mode the split
-// value and dimension of every tile node.
+// [T], nb = 2T 8-bit bucket counters plus a 16-bit first position per four
+// buckets (after the sort: the node tables of a level), a [T] u16 bucket
+// staging array (after the sort, in widest mode: the split dimension of each
+// node of a level), and in widest mode the split value and dimension of
+// every tile node.
 size_t sorted_finisher_smem(int k, int T, int mode, int nb) {
-    size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)2 * nb + (size_t)2 * T;
+    size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)nb + (size_t)nb / 2 + (size_t)2 * T;
     if (mode == KDT_SPLIT_WIDEST) b += (size_t)5 * T;
     return align16(b);
 }
@@ -87,8 +88,9 @@ struct SfSmem {
     uint32_t *keys;   // [k][T], live during the sort
     uint32_t *side;   // [T] partition increment per point, aliases keys after the sort
     uint32_t *idx;    // [T]
-    uint32_t *hist;   // [nb / 2]: two 16-bit bucket counters per word
-    uint32_t *ntab;   // [T/4] node ranges of a level (lo | pos << 16), aliases hist after the sort
+    uint32_t *hist;   // [nb / 4]: four 8-bit bucket counters per word
+    uint16_t *base16; // [nb / 4]: first sorted position of each word's four buckets
+    uint32_t *ntab;   // [T/2] node ranges of a level (lo | pos << 16), aliases hist after the sort
     uint16_t *stage;  // [T] points grouped by bucket, before ranking
     uint8_t *ldim;    // [T/2] split dimension per node of a level, aliases stage (widest mode)
     float *sval;      // [T] split value of tile node (widest mode)
@@ -106,7 +108,8 @@ __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int n
     p += (size_t)4 * T;
     f.hist = reinterpret_cast<uint32_t *>(p);
     f.ntab = f.hist;
-    p += (size_t)2 * nb;
+    f.base16 = reinterpret_cast<uint16_t *>(p + nb);
+    p += (size_t)nb + (size_t)nb / 2;
     f.stage = reinterpret_cast<uint16_t *>(p);
     f.ldim = p;
     p += (size_t)2 * T;
@@ -118,8 +121,8 @@ __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int n
 
 // Super-key order of coordinate c between local points a and b whose x[c]
 // keys are equal: x[c+1 mod k], ..., x[c-1 mod k], then the input index.
-__device__ __forceinline__ bool sk_less_tail(const uint32_t *keys, const uint32_t *idx, int T, int k, int c,
-                                             uint32_t a, uint32_t b) {
+__device__ __noinline__ bool sk_less_tail(const uint32_t *keys, const uint32_t *idx, int T, int k, int c,
+                                          uint32_t a, uint32_t b) {
     for (int i = 1; i < k; ++i) {
         int cc = c + i;
         if (cc >= k) cc -= k;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     const int64_t s0 = full_nodes(a.l0) + tile;
     const uint32_t n = (uint32_t)seg_size(S, a.l0, s0);
     const int64_t base = seg_begin(S, a.l0, s0);
-    if (n < 1u || n > (uint32_t)T || T != E * NT || (uint32_t)nb % (2u * NT) != 0u || nb > 65536) {
+    if (n < 1u || n > (uint32_t)T || T != E * NT || nb != 2 * T) {
         if (tid == 0) {
             set_status(a.status, KDT_EINTERNAL);
             a.fallback[tile] = 0;
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     __syncthreads();
 
     // 2. one reference array per coordinate, sorted by its super key
+    const uint32_t tmask0 = (uint32_t)T - 1u;  // positions stay inside the tile's arrays
     bool fail = false;
     for (int c = 0; c < k; ++c) {
         const uint32_t *kc = sm.keys + c * T;
@@ -282,67 +286,90 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
             fail = true;
             break;
         }
-        for (uint32_t b = tid; b < (uint32_t)nb / 2u; b += NT) sm.hist[b] = 0u;
+        for (uint32_t b = tid; b < (uint32_t)nb / 4u; b += NT) sm.hist[b] = 0u;
         __syncthreads();
+        // bucket and arrival slot of each held point (8-bit counters: a slot
+        // of kSfMaxBucket or more leaves the tile to the select finisher,
+        // before any counter can carry into its neighbour)
         uint32_t pk[E];
+        int big = 0;
 #pragma unroll
         for (int i = 0; i < E; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
             pk[i] = 0u;
             if (q < n) {
                 const uint32_t b = spread ? value_bucket(kc[q], lo, scale, (uint32_t)nb) : 0u;
-                const uint32_t sh = (b & 1u) << 4;
-                pk[i] = (b << 16) | ((atomicAdd(&sm.hist[b >> 1], 1u << sh) >> sh) & 0xffffu);
+                const uint32_t sh = (b & 3u) << 3;
+                const uint32_t r = (atomicAdd(&sm.hist[b >> 2], 1u << sh) >> sh) & 0xffu;
+                big |= r >= (uint32_t)kSfMaxBucket;
+                pk[i] = (b << 16) | r;
             }
-        }
-        __syncthreads();
-        const uint32_t per = (uint32_t)nb / NT;
-        uint16_t *h16 = reinterpret_cast<uint16_t *>(sm.hist);  // counters, then bucket starts
-        uint32_t sum = 0u;
-        int big = 0;
-        for (uint32_t i = 0; i < per; ++i) {
-            const uint32_t h = h16[tid * per + i];
-            sum += h;
-            big |= h > (uint32_t)kSfMaxBucket;
         }
         if (__syncthreads_or(big)) {
             fail = true;
             break;
         }
+        // exclusive scan of the counts: four counter words (16 buckets) per
+        // thread; the first position of each word's buckets goes to base16
+        constexpr uint32_t WPT = 4;  // nb / 4 / NT with nb = 2T = 16 NT
+        uint32_t hw[WPT], sum = 0u;
+#pragma unroll
+        for (uint32_t i = 0; i < WPT; ++i) {
+            hw[i] = sm.hist[tid * WPT + i];
+            sum += (hw[i] * 0x01010101u) >> 24;  // byte sum (each count <= kSfMaxBucket)
+        }
         uint32_t run = block_exclusive_scan(sum, red);
-        for (uint32_t i = 0; i < per; ++i) {
-            const uint32_t h = h16[tid * per + i];
-            h16[tid * per + i] = (uint16_t)run;
-            run += h;
+#pragma unroll
+        for (uint32_t i = 0; i < WPT; ++i) {
+            sm.base16[tid * WPT + i] = (uint16_t)run;
+            run += (hw[i] * 0x01010101u) >> 24;
         }
         __syncthreads();
+        // group the points by bucket; st = first position | size << 16
+        uint32_t st[E];
 #pragma unroll
         for (int i = 0; i < E; ++i) {
             const uint32_t q = tid + (uint32_t)i * NT;
-            if (q < n) sm.stage[h16[pk[i] >> 16] + (pk[i] & 0xffffu)] = (uint16_t)q;
-        }
-        __syncthreads();
-        // rank inside the bucket under the super key of c
-        uint16_t *arr = sm.ids + c * T;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const uint32_t q = tid + (uint32_t)i * NT;
+            st[i] = 0u;
             if (q < n) {
-                const uint32_t b = pk[i] >> 16;
-                const uint32_t beg = h16[b], end = b + 1 < (uint32_t)nb ? h16[b + 1] : n;
-                uint32_t rank = 0u;
-                if (end - beg > 1u) {
-                    const uint32_t kq = kc[q];
-                    for (uint32_t x = beg; x < end; ++x) {
-                        const uint32_t o = sm.stage[x];
-                        const uint32_t ko = kc[o];
-                        rank += (ko < kq || (ko == kq && o != q && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q)))
-                                    ? 1u
-                                    : 0u;
-                    }
-                }
-                arr[beg + rank] = (uint16_t)q;
+                const uint32_t b = pk[i] >> 16, j8 = (b & 3u) << 3;
+                const uint32_t wv = sm.hist[b >> 2];
+                const uint32_t beg = sm.base16[b >> 2] + (((wv * 0x01010100u) >> j8) & 0xffu);  // bytes below b
+                sm.stage[(beg + (pk[i] & 0xffffu)) & tmask0] = (uint16_t)q;
+                st[i] = beg | (((wv >> j8) & 0xffu) << 16);
             }
+        }
+        __syncthreads();
+        // rank inside the bucket under the super key of c; the held points
+        // step through their buckets together, so their loads overlap
+        uint16_t *arr = sm.ids + c * T;
+        uint32_t kq[E], rank[E], smax = 0u;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const uint32_t q = tid + (uint32_t)i * NT;
+            const uint32_t sz = st[i] >> 16;
+            rank[i] = 0u;
+            kq[i] = sz > 1u ? kc[q] : 0u;
+            if (sz > 1u) smax = max(smax, sz);
+        }
+        for (uint32_t j = 0; j < smax; ++j) {
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const uint32_t sz = st[i] >> 16;
+                if (j < sz && sz > 1u) {
+                    const uint32_t q = tid + (uint32_t)i * NT;
+                    const uint32_t o = sm.stage[((st[i] & 0xffffu) + j) & tmask0];
+                    const uint32_t ko = kc[o];
+                    rank[i] += (ko < kq[i] || (ko == kq[i] && o != q && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q)))
+                                   ? 1u
+                                   : 0u;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const uint32_t q = tid + (uint32_t)i * NT;
+            if (q < n) arr[((st[i] & 0xffffu) + rank[i]) & tmask0] = (uint16_t)q;
         }
         __syncthreads();
     }
@@ -543,7 +570,11 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                         if (!((live >> e) & 1u)) continue;
                         const uint32_t t = g[e] << (l + 1);
                         const uint32_t ga = g[e] >> (31 - l);
-                        const int d = sm.ldim[ga ^ (1u << l)];
+                        int d = sm.ldim[ga ^ (1u << l)];
+                        if (d >= k) {  // corrupt table: record it, keep every access in range
+                            set_status(a.status, KDT_EINTERNAL);
+                            d = 0;
+                        }
                         const uint32_t id = sm.ids[d * T + p0 + e] & tmask;
                         sm.side[id] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
                         if (t == 0x80000000u) {
@@ -654,8 +685,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
 int pick_tile(int k, int mode, TilePlan *tp) {
     static const int cands[] = {4096, 2048, 1024, 512};
     for (int T : cands) {
-        const int threads = T / kSfPPT;
-        const int nb = T > 2 * threads ? T : 2 * threads;  // about one point per bucket
+        const int nb = 2 * T;  // about one point per two buckets
         const size_t a = sorted_finisher_smem(k, T, mode, nb);
         const size_t b = select_finisher_smem(k, T, mode);
         if (a <= kSfSmemBudget && b <= kSelectSmemMax) {
@@ -738,9 +768,9 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
         if (nbig < ntiles) {
             SfArgs b2 = a;
             b2.T = Ts;
-            b2.nb = Ts;  // about one point per bucket; a multiple of 2 * (Ts / 8) threads
+            b2.nb = 2 * Ts;
             b2.tile0 = nbig;
-            rc = launch(b2, ntiles - nbig, sorted_finisher_smem(a.k, Ts, a.mode, Ts));
+            rc = launch(b2, ntiles - nbig, sorted_finisher_smem(a.k, Ts, a.mode, 2 * Ts));
             if (rc != KDT_OK) return rc;
         }
     }
