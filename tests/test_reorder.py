@@ -66,7 +66,7 @@ def test_gather_and_inplace_reject_bad_arguments(lib):
     assert lib.kdt_gather_points(fake, 10, 3, fake, None, None) == kdt.EINVAL
     assert lib.kdt_gather_points(fake, 0, 3, fake, other, None) == kdt.EINVAL
     assert lib.kdt_gather_points(fake, 10, 0, fake, other, None) == kdt.EINVAL
-    assert lib.kdt_gather_points(fake, 10, 17, fake, other, None) == kdt.EINVAL
+    assert lib.kdt_gather_points(fake, 10, 33, fake, other, None) == kdt.EINVAL  # k > KDT_MAX_K
     # out overlapping pts
     assert lib.kdt_gather_points(fake, 10, 3, fake, ctypes.c_void_p(0x1000 + 40), None) == kdt.EINVAL
     assert lib.kdt_gather_points(ctypes.c_void_p(0x1000 + 40), 10, 3, fake, fake, None) == kdt.EINVAL
