@@ -35,11 +35,11 @@ constexpr int kInitPPT = 4;  // points per thread per iteration
 
 // KM: compile-time bound on k (4, 8, 16 or 32), so that the per-dimension
 // minima and maxima stay in registers without reserving 2 * KDT_MAX_K of them
-// for small k.
+// for small k.  Each point's record (keys, then its input index) is written
+// whole: for k <= 3 one 16-byte store, otherwise four words at a time.
 template <int KM>
 __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restrict__ pts, int64_t N,
-                                                            int k, int64_t ld, uint32_t *__restrict__ keys,
-                                                            uint32_t *__restrict__ idx,
+                                                            int k, int64_t ld, uint4 *__restrict__ rec,
                                                             uint32_t *__restrict__ bbox,
                                                             int *__restrict__ status) {
     uint32_t mn[KM], mx[KM];
@@ -51,34 +51,69 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
     int bad = 0;
     const int64_t nt = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < N; i0 += nt * kInitPPT) {
-        // one dimension at a time: the kInitPPT loads go out before the stores
+        if (KM == 4) {
+            // the kInitPPT points' loads go out before the stores, one
+            // dimension at a time (coalesced across the warp)
+            uint4 r[kInitPPT];
 #pragma unroll
-        for (int c = 0; c < KM; ++c) {
-            if (c < k) {
-                float f[kInitPPT];
+            for (int u = 0; u < kInitPPT; ++u) r[u] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int u = 0; u < kInitPPT; ++u) {
-                    const int64_t i = i0 + u * nt;
-                    f[u] = i < N ? __ldg(pts + i * k + c) : 0.f;
-                }
+            for (int c = 0; c < 4; ++c) {
+                if (c < k) {
+                    float f[kInitPPT];
 #pragma unroll
-                for (int u = 0; u < kInitPPT; ++u) {
-                    const int64_t i = i0 + u * nt;
-                    if (i < N) {
-                        bad |= !isfinite(f[u]);
-                        const uint32_t key = f2key(f[u]);
-                        keys[(int64_t)c * ld + i] = key;
-                        mn[c] = min(mn[c], key);
-                        mx[c] = max(mx[c], key);
+                    for (int u = 0; u < kInitPPT; ++u) {
+                        const int64_t i = i0 + u * nt;
+                        f[u] = i < N ? __ldg(pts + i * k + c) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kInitPPT; ++u) {
+                        if (i0 + u * nt < N) {
+                            bad |= !isfinite(f[u]);
+                            const uint32_t key = f2key(f[u]);
+                            u4_set(r[u], c, key);
+                            mn[c] = min(mn[c], key);
+                            mx[c] = max(mx[c], key);
+                        }
                     }
                 }
             }
-        }
-        if (idx != nullptr) {
 #pragma unroll
             for (int u = 0; u < kInitPPT; ++u) {
                 const int64_t i = i0 + u * nt;
-                if (i < N) idx[i] = (uint32_t)i;
+                if (i < N) {
+                    u4_set(r[u], k, (uint32_t)i);
+                    rec[i] = r[u];
+                }
+            }
+        } else {
+            // words 0..k of each record: keys, then the index; a group is
+            // stored once its four words (or the last, word k) are set
+#pragma unroll
+            for (int u = 0; u < kInitPPT; ++u) {
+                const int64_t i = i0 + u * nt;
+                if (i >= N) continue;
+                uint4 r = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int wd = 0; wd <= KM; ++wd) {
+                    if (wd > k) break;
+                    if (wd < k) {
+                        const float f = __ldg(pts + i * k + wd);
+                        bad |= !isfinite(f);
+                        const uint32_t key = f2key(f);
+                        if (wd < KM) {
+                            mn[wd] = min(mn[wd], key);
+                            mx[wd] = max(mx[wd], key);
+                        }
+                        u4_set(r, wd & 3, key);
+                    } else {
+                        u4_set(r, wd & 3, (uint32_t)i);
+                    }
+                    if ((wd & 3) == 3 || wd == k) {
+                        rec[(int64_t)(wd >> 2) * ld + i] = r;
+                        r = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
             }
         }
     }
@@ -136,13 +171,11 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     off = align_up(off + 64, 256);
     q.off_bbox = off;
     off = align_up(off + (size_t)2 * k * 4, 256);
-    q.ld = (N + 7) & ~(int64_t)7;  // multiple of 4 words: 128-bit loads stay aligned
+    q.ld = (N + 7) & ~(int64_t)7;
     for (int b = 0; b < 3; ++b) {
         const int64_t rows = (b < 2 || lf > 0) ? q.ld : 0;
-        q.off_keys[b] = off;
-        off = align_up(off + (size_t)k * rows * 4, 256);
-        q.off_idx[b] = off;
-        off = align_up(off + (size_t)rows * 4, 256);
+        q.off_rec[b] = off;
+        off = align_up(off + (size_t)rec_groups(k) * rows * 16, 256);
     }
     for (int b = 0; b < 2; ++b) {
         q.off_dom[b] = off;
@@ -166,10 +199,7 @@ Buffers carve(const Plan &p, void *base) {
     Buffers r;
     r.status = reinterpret_cast<int *>(b + p.off_status);
     r.bbox = reinterpret_cast<uint32_t *>(b + p.off_bbox);
-    for (int i = 0; i < 3; ++i) {
-        r.keys[i] = reinterpret_cast<uint32_t *>(b + p.off_keys[i]);
-        r.idx[i] = reinterpret_cast<uint32_t *>(b + p.off_idx[i]);
-    }
+    for (int i = 0; i < 3; ++i) r.rec[i] = reinterpret_cast<uint4 *>(b + p.off_rec[i]);
     for (int i = 0; i < 2; ++i) {
         r.dom[i] = reinterpret_cast<float *>(b + p.off_dom[i]);
         r.dim[i] = reinterpret_cast<int *>(b + p.off_dim[i]);
@@ -201,21 +231,18 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 16;
         if (blocks > cap) blocks = cap;
         ProfScope ps(stream, "init", 0.0);
-        // the input-index column starts as the identity: written only if the
-        // finisher takes the root subtree (global levels use the position)
-        uint32_t *idx0 = p.finish_level == 0 ? b.idx[0] : nullptr;
-        if (k <= 4)
-            init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0, b.bbox,
+        if (k <= 3)
+            init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);
         else if (k <= 8)
-            init_kernel<8><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0, b.bbox,
+            init_kernel<8><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);
         else if (k <= 16)
-            init_kernel<16><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0,
-                                                                           b.bbox, b.status);
+            init_kernel<16><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+                                                                           b.status);
         else
-            init_kernel<32><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.keys[0], idx0,
-                                                                           b.bbox, b.status);
+            init_kernel<32><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+                                                                           b.status);
         KDT_LAUNCH_CHECK();
     }
     {

@@ -37,7 +37,7 @@ struct FinArgs {
     Shape S;
     int k, mode, l0, T;
     int64_t ld;
-    const uint32_t *src_keys, *src_idx;
+    const uint4 *src;  // records of level l0 (group columns of ld records)
     int32_t *perm;
     const float *dom;  // node table of level l0
     const uint8_t *only;  // per tile: nonzero = finish it here
@@ -497,18 +497,25 @@ __global__ void __launch_bounds__(kFinThreads, 2) finisher_kernel(FinArgs a) {
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    // load the tile: all loads of a batch are issued before its stores
-    for (int c = 0; c <= k; ++c) {
-        const uint32_t *col = (c < k ? a.src_keys + (int64_t)c * a.ld : a.src_idx) + base;
-        uint32_t *dstc = c < k ? sm.keys + c * a.T : sm.idx;
-        const uint32_t nt = blockDim.x;
+    const uint32_t nt = blockDim.x;
+    // load the tile's records: words 0..k-1 to the key arrays, word k to
+    //    the input indices (G uint4 per record; a batch's loads go out first)
+    for (int gi = 0; gi < rec_groups(k); ++gi) {
+        const uint4 *col = a.src + (int64_t)gi * a.ld + base;
         for (uint32_t q = tid; q < n; q += 4 * nt) {
-            uint32_t v[4];
+            uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = q + u * nt < n ? __ldg(col + q + u * nt) : 0u;
+            for (int u = 0; u < 4; ++u) v[u] = q + u * nt < n ? __ldg(col + q + u * nt) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (q + u * nt < n) dstc[q + u * nt] = v[u];
+            for (int u = 0; u < 4; ++u) {
+                if (q + u * nt >= n) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int wd = 4 * gi + j;
+                    if (wd < k) sm.keys[wd * a.T + q + u * nt] = u4_word(v[u], j);
+                    else if (wd == k) sm.idx[q + u * nt] = u4_word(v[u], j);
+                }
+            }
         }
     }
     for (uint32_t q = tid; q < n; q += blockDim.x) sm.ids[0][q] = (uint16_t)q;
@@ -596,8 +603,7 @@ int launch_select_finisher(const Plan &p, const Buffers &b, int src, int32_t *pe
     a.l0 = p.finish_level;
     a.T = p.tp.tile;
     a.ld = p.ld;
-    a.src_keys = b.keys[src];
-    a.src_idx = b.idx[src];
+    a.src = b.rec[src];
     a.perm = perm;
     a.dom = b.dom[p.finish_level & 1];
     a.only = only;

@@ -52,7 +52,8 @@ namespace kdt {
 
 constexpr int kSfPPT = 8;          // positions (sort points) per thread: T = kSfPPT * threads
 constexpr int kSfMaxBucket = 16;   // larger buckets leave the tile to the select finisher
-constexpr size_t kSfSmemBudget = 110 * 1024;  // two 512-thread CTAs per SM
+constexpr size_t kSfSmemBudget = 110 * 1024;   // two CTAs of up to 512 threads per SM
+constexpr size_t kSfSmemBudget1 = 224 * 1024;  // one 1024-thread CTA per SM (T = 8192)
 constexpr int kMaxLevels = 32;
 constexpr uint32_t kSegHead = 0x80000000u;  // scan word: a node range starts inside the scanned span
 
@@ -61,7 +62,7 @@ struct SfArgs {
     int k, mode, l0, T, nb;
     int64_t tile0;       // this launch's first tile (subtree of level l0, counted from the level's first)
     int64_t ld;
-    const uint32_t *src_keys, *src_idx;
+    const uint4 *src;    // records of level l0 (group columns of ld records)
     int32_t *perm;
     const float *dom;    // node table of level l0 (widest mode)
     uint8_t *fallback;   // per tile: 1 = left to the select finisher
@@ -247,17 +248,24 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         return;
     }
 
-    // 1. load the tile: all loads of a batch are issued before its stores
-    for (int c = 0; c <= k; ++c) {
-        const uint32_t *col = (c < k ? a.src_keys + (int64_t)c * a.ld : a.src_idx) + base;
-        uint32_t *dstc = c < k ? sm.keys + c * T : sm.idx;
+    // 1. load the tile's records: words 0..k-1 to the key arrays, word k to
+    //    the input indices (G uint4 per record; a batch's loads go out first)
+    for (int gi = 0; gi < rec_groups(k); ++gi) {
+        const uint4 *col = a.src + (int64_t)gi * a.ld + base;
         for (uint32_t q = tid; q < n; q += 4 * NT) {
-            uint32_t v[4];
+            uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = q + u * NT < n ? __ldg(col + q + u * NT) : 0u;
+            for (int u = 0; u < 4; ++u) v[u] = q + u * NT < n ? __ldg(col + q + u * NT) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (q + u * NT < n) dstc[q + u * NT] = v[u];
+            for (int u = 0; u < 4; ++u) {
+                if (q + u * NT >= n) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int wd = 4 * gi + j;
+                    if (wd < k) sm.keys[wd * T + q + u * NT] = u4_word(v[u], j);
+                    else if (wd == k) sm.idx[q + u * NT] = u4_word(v[u], j);
+                }
+            }
         }
     }
     __syncthreads();
@@ -579,7 +587,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                         sm.side[id] = t == 0x80000000u ? 0u : ((t >> 31) ? 0x10000u : 1u);
                         if (t == 0x80000000u) {
                             const uint32_t ib = id < n ? id : 0u;  // a permutation of [0, n) unless corrupt
-                            sm.sval[ga - 1u] = key2f(__ldg(a.src_keys + (int64_t)d * a.ld + base + ib));
+                            sm.sval[ga - 1u] = key2f(rec_word(a.src, a.ld, d, base + ib));
                             sm.sdim[ga - 1u] = (uint8_t)d;
                         }
                     }
@@ -679,16 +687,17 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     }
 }
 
-// Tile size T: the largest candidate whose sorted-finisher CTA (T / 8
-// threads) fits two per SM and whose select-finisher CTA (the fallback for the
-// same tiles) fits one.
+// Tile size T: 8192 if its sorted-finisher CTA (1024 threads) fits one per
+// SM, else the largest candidate whose CTA (T / 8 threads) fits two per SM;
+// the select-finisher CTA (the fallback for the same tiles) must fit one.
+// Every global level a larger tile absorbs is a whole-array pass saved.
 int pick_tile(int k, int mode, TilePlan *tp) {
-    static const int cands[] = {4096, 2048, 1024, 512};
+    static const int cands[] = {8192, 4096, 2048, 1024, 512};
     for (int T : cands) {
         const int nb = 2 * T;  // about one point per two buckets
         const size_t a = sorted_finisher_smem(k, T, mode, nb);
         const size_t b = select_finisher_smem(k, T, mode);
-        if (a <= kSfSmemBudget && b <= kSelectSmemMax) {
+        if (a <= (T == 8192 ? kSfSmemBudget1 : kSfSmemBudget) && b <= kSelectSmemMax) {
             tp->tile = T;
             tp->nb = nb;
             tp->smem = a;
@@ -726,8 +735,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     a.T = p.tp.tile;
     a.nb = p.tp.nb;
     a.ld = p.ld;
-    a.src_keys = b.keys[src];
-    a.src_idx = b.idx[src];
+    a.src = b.rec[src];
     a.perm = perm;
     a.dom = b.dom[p.finish_level & 1];
     a.fallback = b.fallback;
@@ -754,6 +762,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
         auto launch = [&](const SfArgs &x, int64_t n_tiles, size_t smem) -> int {
             if (n_tiles <= 0) return KDT_OK;
             switch (x.T / kSfPPT) {
+                case 1024: return launch_sorted<1024>(x, n_tiles, smem, stream);
                 case 512: return launch_sorted<512>(x, n_tiles, smem, stream);
                 case 256: return launch_sorted<256>(x, n_tiles, smem, stream);
                 case 128: return launch_sorted<128>(x, n_tiles, smem, stream);

@@ -80,9 +80,9 @@ int enqueue_gather(const float *pts, int64_t N, int k, const int32_t *perm, floa
 int enqueue_inplace_tail(const Plan &p, const Buffers &b, float *pts, const int32_t *perm, cudaStream_t stream) {
     const int64_t N = p.S.N;
     const int k = p.k;
-    // after the build every record buffer is free; buffer 0's key columns
-    // (k * ld >= N * k words) hold the reordered rows until they are copied back
-    uint32_t *tmp = b.keys[0];
+    // after the build every record buffer is free; buffer 0 (G * 4 * ld >=
+    // (k + 1) * N words) holds the reordered rows until they are copied back
+    uint32_t *tmp = reinterpret_cast<uint32_t *>(b.rec[0]);
     {
         ProfScope ps(stream, "gather", (double)N * (4.0 + 8.0 * k));
         launch_gather(reinterpret_cast<const uint32_t *>(pts), N, k, perm, tmp, b.status, b.status, KDT_EINTERNAL,

@@ -129,6 +129,31 @@ __device__ __forceinline__ int widest_dim(const float *lo, const float *hi, int 
     return best;
 }
 
+// ---- point records -----------------------------------------------------------
+// On the global levels a point travels as a record of words: its k order-
+// preserving keys (words 0..k-1) and its input index (word k), grouped four
+// to a 16-byte uint4.  A record buffer holds G = ceil((k+1)/4) group columns
+// of ld uint4 each -- group g of record q at g * ld + q -- so for k <= 3 a
+// whole record is one 128-bit load or store (padding words are unused).
+
+__host__ __device__ __forceinline__ int rec_groups(int k) { return (k + 4) / 4; }
+
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ void u4_set(uint4 &v, int i, uint32_t x) {
+    if (i == 0) v.x = x;
+    else if (i == 1) v.y = x;
+    else if (i == 2) v.z = x;
+    else v.w = x;
+}
+
+// Word w of record q.
+__device__ __forceinline__ uint32_t rec_word(const uint4 *r, int64_t ld, int w, int64_t q) {
+    return reinterpret_cast<const uint32_t *>(r + (int64_t)(w >> 2) * ld + q)[w & 3];
+}
+
 // ---- device status ----------------------------------------------------------
 
 __device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
@@ -167,9 +192,9 @@ struct Plan {
     int64_t table_cap;   // node-table entries per level
     int64_t hist_rows;   // histogram rows per buffer (multi-CTA levels)
     int64_t sel_cap;     // SegSel entries
-    int64_t ld;          // column stride of the record buffers (N rounded up to 8)
+    int64_t ld;          // records per group column (N rounded up to 8)
     // byte offsets inside the workspace
-    size_t off_status, off_bbox, off_keys[3], off_idx[3], off_dom[2], off_dim[2], off_hist[2], off_sel, off_fb;
+    size_t off_status, off_bbox, off_rec[3], off_dom[2], off_dim[2], off_hist[2], off_sel, off_fb;
     size_t bytes;
 };
 
@@ -178,8 +203,7 @@ int make_plan(int64_t N, int k, int mode, Plan *p);
 struct Buffers {
     int *status;
     uint32_t *bbox;  // [2k]: min keys then max keys
-    uint32_t *keys[3];  // record buffers: [0], [1] ping-pong, [2] bucket candidates
-    uint32_t *idx[3];
+    uint4 *rec[3];   // record buffers: [0], [1] ping-pong, [2] bucket candidates
     float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
     int *dim[2];
     uint32_t *hist[2];  // [rows][kBuckets]

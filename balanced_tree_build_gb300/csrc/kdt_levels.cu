@@ -35,7 +35,6 @@ constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
 constexpr int kEPT = 4;                          // consecutive points per thread per tile
 constexpr int kPartThreads = 128;                // partition CTAs (multi-CTA and per-subtree)
-constexpr int kPre = 4;                          // key columns loaded ahead in a tile
 constexpr int kTile = kPartThreads * kEPT;
 
 // ---- value buckets ----------------------------------------------------------
@@ -108,9 +107,9 @@ __device__ __forceinline__ int64_t seg_of_pos(const Shape &S, int l, int64_t p) 
 struct LevelArgs {
     Shape S;
     int k, mode, l;
-    const uint32_t *src_keys, *src_idx;
-    uint32_t *dst_keys, *dst_idx;
-    uint32_t *cand_keys, *cand_idx;
+    const uint4 *src;    // records of this level (G group columns of ld records)
+    uint4 *dst, *cand;   // records of the next level; candidates of the split buckets
+    int G;               // record groups: ceil((k + 1) / 4)
     int32_t *perm;
     const float *dom_cur;
     const int *dim_cur;
@@ -121,7 +120,7 @@ struct LevelArgs {
     SegSel *sel;
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
-    int64_t ld;          // column stride of the record buffers
+    int64_t ld;          // records per group column
 };
 
 struct SegInfo {
@@ -193,28 +192,16 @@ struct PartPlan {
     int64_t right_tail;  // first position of the certain-right group
 };
 
-// Loads the 4 consecutive words at col[q0 .. q0+4) (q0 a multiple of 4) as
-// one 128-bit load.
-__device__ __forceinline__ void load4(const uint32_t *col, int64_t q0, uint32_t *v) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(col + q0));
-    v[0] = x.x;
-    v[1] = x.y;
-    v[2] = x.z;
-    v[3] = x.w;
-}
-
-// Prefetches the record lines of the tile starting at t0 (a multiple of 4,
-// clipped to ve) into L2, so that the tile's loads, issued two tiles later,
-// wait on L2 rather than DRAM: one 128-byte line per thread and column.
+// Prefetches the record lines of the tile starting at t0 (clipped to ve)
+// into L2, so that the tile's loads, issued two tiles later, wait on L2
+// rather than DRAM: one 128-byte line (8 records) per thread and group.
 __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve) {
-    const uint32_t lines = kTile / 32;  // 128-byte lines per column
-    for (uint32_t t = threadIdx.x; t < (uint32_t)(a.k + 1) * lines; t += blockDim.x) {
-        const uint32_t c = t / lines;
-        const int64_t q = t0 + (int64_t)(t - c * lines) * 32;
+    const uint32_t lines = kTile / 8;  // 128-byte lines per group column
+    for (uint32_t t = threadIdx.x; t < (uint32_t)a.G * lines; t += blockDim.x) {
+        const uint32_t gi = t / lines;
+        const int64_t q = t0 + (int64_t)(t - gi * lines) * 8;
         if (q >= ve) continue;
-        const uint32_t *col = (int)c < a.k ? a.src_keys + (int64_t)c * a.ld : a.src_idx;
-        if (col == nullptr) continue;  // level 0: no index column
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(col + q));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.src + (int64_t)gi * a.ld + q));
     }
 }
 
@@ -234,157 +221,111 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
                           const Bucketer &bkc, int dn) {
     // positions are below 2^31 (N < 2^31): 32-bit arithmetic from here on
     const int64_t ld = a.ld;
-    const int k = a.k, d = g.d;
+    const int d = g.d;
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
     const uint32_t lt = (1u << lane) - 1u;
     const uint32_t q0 = (uint32_t)t0 + 4u * tid;
     const uint32_t vb32 = (uint32_t)vb, ve32 = (uint32_t)ve;
     const bool any = q0 + 4u > vb32 && q0 < ve32;
-    uint32_t pv[kPre + 1][kEPT];
+    // group 0 of the thread's four records (for k <= 3 the whole record);
+    // rows up to q0 + 3 < ld exist in every buffer
+    uint4 r[kEPT];
 #pragma unroll
-    for (int c = 0; c <= kPre; ++c) {
-#pragma unroll
-        for (int i = 0; i < kEPT; ++i) pv[c][i] = 0u;
-        if (c == kPre && a.src_idx == nullptr) {  // level 0: the input index is the position
-#pragma unroll
-            for (int i = 0; i < kEPT; ++i) pv[c][i] = q0 + (uint32_t)i;
-            continue;
-        }
-        if (any && (c == kPre || c < k)) load4(c == kPre ? a.src_idx : a.src_keys + (int64_t)c * ld, q0, pv[c]);
-    }
+    for (int i = 0; i < kEPT; ++i) r[i] = any ? __ldg(a.src + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t kx[kEPT];
-    if (d < kPre) {
 #pragma unroll
-        for (int i = 0; i < kEPT; ++i) {
-            uint32_t key = pv[0][i];  // static indices keep pv in registers
-#pragma unroll
-            for (int c = 1; c < kPre; ++c)
-                if (d == c) key = pv[c][i];
-            kx[i] = key;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < kEPT; ++i) kx[i] = 0u;
-        if (any) load4(a.src_keys + (int64_t)d * ld, q0, kx);
-    }
-    uint32_t mL[kEPT], mR[kEPT], mC[kEPT];
-    uint32_t tL = 0, tC = 0, tR = 0;
+    for (int i = 0; i < kEPT; ++i)
+        kx[i] = d < 4 ? u4_word(r[i], d) : (any ? rec_word(a.src, ld, d, q0 + i) : 0u);
+    // certain points: two ballots per point (certain, right); the
+    // candidates of the split bucket (a few per thousand) are reserved per
+    // warp straight from the candidate cursor
+    uint32_t mV[kEPT], mR[kEPT];
+    uint32_t tL = 0, tR = 0;
+    int side[kEPT];
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         const uint32_t q = q0 + (uint32_t)i;
-        int side = 3;
-        if (q >= vb32 && q < ve32) side = kx[i] < pp.klo ? 0 : (kx[i] >= pp.khi ? 2 : 1);  // bucket vs b*
-        mL[i] = __ballot_sync(0xffffffffu, side == 0);
-        mC[i] = __ballot_sync(0xffffffffu, side == 1);
-        mR[i] = __ballot_sync(0xffffffffu, side == 2);
-        tL += __popc(mL[i]);
-        tC += __popc(mC[i]);
+        side[i] = 3;
+        if (q >= vb32 && q < ve32) side[i] = kx[i] < pp.klo ? 0 : (kx[i] >= pp.khi ? 2 : 1);  // bucket vs b*
+        mV[i] = __ballot_sync(0xffffffffu, side[i] == 0 || side[i] == 2);
+        mR[i] = __ballot_sync(0xffffffffu, side[i] == 2);
+        tL += __popc(mV[i] & ~mR[i]);
         tR += __popc(mR[i]);
     }
     if (lane == 0) {
-        wtot[3 * w + 0] = tL;
-        wtot[3 * w + 1] = tC;
-        wtot[3 * w + 2] = tR;
+        wtot[2 * w + 0] = tL;
+        wtot[2 * w + 1] = tR;
     }
     __syncthreads();
-    if (w == 0) {
-        // exclusive prefix over warps, then one reservation per side
-        uint32_t v[3], x[3];
-#pragma unroll
-        for (int sd = 0; sd < 3; ++sd) {
-            v[sd] = lane < nw ? wtot[3 * lane + sd] : 0u;
-            x[sd] = v[sd];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, x[sd], o);
-                if (lane >= (uint32_t)o) x[sd] += y;
-            }
-        }
-        uint32_t base[3] = {0u, 0u, 0u};
-        if (lane == 31) {
-#pragma unroll
-            for (int sd = 0; sd < 3; ++sd) base[sd] = x[sd] ? atomicAdd(&cursors[sd], x[sd]) : 0u;
-        }
-#pragma unroll
-        for (int sd = 0; sd < 3; ++sd) {
-            base[sd] = __shfl_sync(0xffffffffu, base[sd], 31);
-            if (lane < nw) wbase[3 * lane + sd] = base[sd] + x[sd] - v[sd];
+    if (tid < 2u) {  // side tid: one cursor reservation, then the warps' offsets
+        uint32_t sum = 0u;
+        for (uint32_t v = 0; v < nw; ++v) sum += wtot[2 * v + tid];
+        uint32_t base = sum ? atomicAdd(&cursors[tid ? 2 : 0], sum) : 0u;
+        for (uint32_t v = 0; v < nw; ++v) {
+            wbase[2 * v + tid] = base;
+            base += wtot[2 * v + tid];
         }
     }
     __syncthreads();
-    uint32_t oL = wbase[3 * w + 0], oC = wbase[3 * w + 1], oR = wbase[3 * w + 2];
+    uint32_t oL = wbase[2 * w + 0], oR = wbase[2 * w + 1];
     const uint32_t lbeg = (uint32_t)g.left_begin, rtail = (uint32_t)pp.right_tail;
     const uint32_t cgap = lbeg + pp.below, s32 = (uint32_t)g.s;
-    // pos: destination position of each point (32 bit); side 3 = not stored;
-    // candidates (side 1, rare) are stored separately below
+    // pos: destination position of each point (32 bit); side 3 = not stored
     uint32_t pos[kEPT];
-    int side[kEPT];
-    bool anyc = false;
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         pos[i] = 0u;
-        side[i] = 3;
-        const uint32_t bit = 1u << lane;
+        const uint32_t mL = mV[i] & ~mR[i];
         bool ok = true;
-        if (mL[i] & bit) {
-            const uint32_t o = oL + __popc(mL[i] & lt);
+        if (side[i] == 0) {
+            const uint32_t o = oL + __popc(mL & lt);
             ok = o < pp.below;
             pos[i] = lbeg + o;
-            side[i] = 0;
-        } else if (mR[i] & bit) {
+        } else if (side[i] == 2) {
             const uint32_t o = oR + __popc(mR[i] & lt);
             ok = o < pp.above;
             pos[i] = rtail + o;
-            side[i] = 2;
-        } else if (mC[i] & bit) {
-            const uint32_t o = oC + __popc(mC[i] & lt);
-            ok = o < pp.cnt;
-            pos[i] = o + 1u < pp.cnt ? cgap + o : s32;  // candidate slot o: the gap, the last one position s
-            side[i] = 1;
-            anyc = true;
         }
-        oL += __popc(mL[i]);
-        oC += __popc(mC[i]);
+        oL += __popc(mL);
         oR += __popc(mR[i]);
+        const uint32_t cm = __ballot_sync(0xffffffffu, side[i] == 1);
+        if (cm) {
+            const int leader = __ffs((int)cm) - 1;
+            uint32_t cb = 0u;
+            if ((int)lane == leader) cb = atomicAdd(&cursors[1], (uint32_t)__popc(cm));
+            cb = __shfl_sync(0xffffffffu, cb, leader);
+            if (side[i] == 1) {
+                const uint32_t o = cb + __popc(cm & lt);
+                ok = o < pp.cnt;
+                pos[i] = o + 1u < pp.cnt ? cgap + o : s32;  // candidate slot o: the gap, the last one position s
+            }
+        }
         if (!ok) {
             set_status(a.status, KDT_EINTERNAL);
             side[i] = 3;
         }
     }
-    // stores: preloaded words first, then (k > kPre) the remaining columns
+    // stores: group 0 from registers, then the other groups (k >= 4)
 #pragma unroll
-    for (int c = 0; c <= kPre; ++c) {
-        if (c < kPre && c >= k) continue;
-        uint32_t *dcol = c == kPre ? a.dst_idx : a.dst_keys + (int64_t)c * ld;
-#pragma unroll
-        for (int i = 0; i < kEPT; ++i) {
-            if (side[i] == 0 || side[i] == 2) {
-                dcol[pos[i]] = pv[c][i];
-                // pv[kPre] is the input index, not key column kPre
-                if (fh != nullptr && c < kPre && c == dn)
-                    atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(pv[c][i])], 1u);
-            }
-        }
-        if (anyc) {
-            uint32_t *ccol = c == kPre ? a.cand_idx : a.cand_keys + (int64_t)c * ld;
-#pragma unroll
-            for (int i = 0; i < kEPT; ++i)
-                if (side[i] == 1) ccol[pos[i]] = pv[c][i];
+    for (int i = 0; i < kEPT; ++i) {
+        if (side[i] == 0 || side[i] == 2) {
+            a.dst[pos[i]] = r[i];
+            if (fh != nullptr && dn < 4) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(u4_word(r[i], dn))], 1u);
+        } else if (side[i] == 1) {
+            a.cand[pos[i]] = r[i];
         }
     }
-    for (int c = kPre; c < k; ++c) {
-        uint32_t *dcol = a.dst_keys + (int64_t)c * ld;
-        uint32_t *ccol = a.cand_keys + (int64_t)c * ld;
-        uint32_t v[kEPT];
+    for (int gi = 1; gi < a.G; ++gi) {
+        uint4 v[kEPT];
 #pragma unroll
-        for (int i = 0; i < kEPT; ++i) v[i] = 0u;
-        if (any) load4(a.src_keys + (int64_t)c * ld, q0, v);
+        for (int i = 0; i < kEPT; ++i) v[i] = any ? __ldg(a.src + (int64_t)gi * ld + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int i = 0; i < kEPT; ++i) {
             if (side[i] == 3) continue;
-            (side[i] == 1 ? ccol : dcol)[pos[i]] = v[i];
-            if (fh != nullptr && c == dn && side[i] != 1) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(v[i])], 1u);
+            (side[i] == 1 ? a.cand : a.dst)[(int64_t)gi * ld + pos[i]] = v[i];
+            if (fh != nullptr && (dn >> 2) == gi && side[i] != 1)
+                atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(u4_word(v[i], dn & 3))], 1u);
         }
     }
 }
@@ -393,17 +334,16 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
 
 // Word i of candidate slot q (split order of dimension d).
 struct CandAcc {
-    const uint32_t *keys, *idx;
-    int64_t ld, gap_begin, s;  // ld: column stride
+    const uint4 *rec;
+    int64_t ld, gap_begin, s;  // ld: records per group column
     uint32_t cnt;
     int k, d;
     __device__ __forceinline__ int64_t pos(uint32_t q) const { return q + 1u < cnt ? gap_begin + q : s; }
     __device__ __forceinline__ uint32_t operator()(int i, uint32_t q) const {
-        const int64_t p = pos(q);
-        if (i == k) return idx[p];
         int c = d + i;
-        if (c >= k) c -= k;
-        return keys[(int64_t)c * ld + p];
+        if (i == k) c = k;  // the input index
+        else if (c >= k) c -= k;
+        return rec_word(rec, ld, c, pos(q));
     }
 };
 
@@ -417,7 +357,7 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
     const int k = a.k;
     const int64_t ld = a.ld;
     const uint32_t r = g.m - pp.below;  // rank of the split point among the candidates
-    const CandAcc acc{a.cand_keys, a.cand_idx, ld, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
+    const CandAcc acc{a.cand, ld, g.left_begin + pp.below, g.s, pp.cnt, k, g.d};
     if (pp.cnt <= 32u) {  // a few candidates (deep levels): one warp selects, no CTA barriers per round
         if (tid < 32u) group_select(WarpsGroup{0u, 32u, 1}, acc, pp.cnt, r, k + 1, st, hist, kWarpRadixBits, red);
         __syncthreads();
@@ -491,17 +431,16 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
                 }
             }
         }
-        for (int c = 0; c <= k; ++c) {
-            const uint32_t *scol = c < k ? a.cand_keys + (int64_t)c * ld : a.cand_idx;
-            uint32_t *dcol = c < k ? a.dst_keys + (int64_t)c * ld : a.dst_idx;
-            uint32_t v[kRB];
+        for (int gi = 0; gi < a.G; ++gi) {
+            uint4 v[kRB];
 #pragma unroll
-            for (int u = 0; u < kRB; ++u) v[u] = side[u] >= 0 ? scol[sp[u]] : 0u;
+            for (int u = 0; u < kRB; ++u) v[u] = side[u] >= 0 ? a.cand[(int64_t)gi * ld + sp[u]] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int u = 0; u < kRB; ++u) {
                 if (side[u] < 0) continue;
-                dcol[pos[u]] = v[u];
-                if (fuse && c == dn) atomicAdd(&a.hist_nxt[(2 * g.j + side[u]) * kBuckets + bkc(v[u])], 1u);
+                a.dst[(int64_t)gi * ld + pos[u]] = v[u];
+                if (fuse && (dn >> 2) == gi)
+                    atomicAdd(&a.hist_nxt[(2 * g.j + side[u]) * kBuckets + bkc(u4_word(v[u], dn & 3))], 1u);
             }
         }
     }
@@ -541,8 +480,9 @@ __device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t 
     return total == n;
 }
 
-// Histogram of the bucket function over col[b, e) into shared `hist`; each
-// thread issues eight loads before its atomics (keys are in global memory).
+// Histogram of the bucket function over word d of records [b, e) into shared
+// `hist`; each thread issues eight loads before its atomics (the records are
+// in global memory; col points at word d of record 0, stride 4 words).
 __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64_t e, const Bucketer &bk,
                                            uint32_t *hist) {
     constexpr int kH = 8;
@@ -552,7 +492,7 @@ __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64
 #pragma unroll
         for (int u = 0; u < kH; ++u) {
             const int64_t q = q0 + (int64_t)u * nt;
-            v[u] = q < e ? __ldg(col + q) : 0u;
+            v[u] = q < e ? __ldg(col + 4 * q) : 0u;
         }
 #pragma unroll
         for (int u = 0; u < kH; ++u)
@@ -576,7 +516,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
         const Bucketer bk = seg_bucketer(a, g.j, g.d);
         for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        const uint32_t *col = a.src_keys + (int64_t)g.d * ld;
+        const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
         hist_range(col, p, pe, bk, hist);
         __syncthreads();
         uint32_t *H = a.hist_cur + g.j * kBuckets;
@@ -630,7 +570,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
 }
 
 __global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a) {
-    __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
+    __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
     if (stop_requested(a.status, &stop)) return;
@@ -693,7 +633,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t red[64];
-    __shared__ uint32_t wtot[3 * 32], wbase[3 * 32];
+    __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t cursors[3];
     __shared__ uint32_t medw[kMaxWords];
     __shared__ uint32_t cur2[2];
@@ -704,7 +644,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     const SegInfo g = seg_info(a, s);
     const Bucketer bk = seg_bucketer(a, g.j, g.d);
     const int64_t ld = a.ld;
-    const uint32_t *col = a.src_keys + (int64_t)g.d * ld;
+    const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
     for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
     if (threadIdx.x < 3) cursors[threadIdx.x] = 0u;
     __syncthreads();
@@ -744,12 +684,10 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.k = k;
     a.mode = p.mode;
     a.l = l;
-    a.src_keys = b.keys[src];
-    a.src_idx = l == 0 ? nullptr : b.idx[src];  // level 0 reads no index column: it is the position
-    a.dst_keys = b.keys[src ^ 1];
-    a.dst_idx = b.idx[src ^ 1];
-    a.cand_keys = b.keys[2];
-    a.cand_idx = b.idx[2];
+    a.src = b.rec[src];
+    a.dst = b.rec[src ^ 1];
+    a.cand = b.rec[2];
+    a.G = rec_groups(k);
     a.perm = perm;
     a.dom_cur = b.dom[l & 1];
     a.dim_cur = b.dim[l & 1];
