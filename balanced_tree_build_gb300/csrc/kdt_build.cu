@@ -164,7 +164,9 @@ int make_plan(int64_t N, int k, int mode, Plan *p) {
     while (lm < lf && ((int64_t)1 << lm) <= kMultiMaxSegs) ++lm;
     q.multi_levels = lm;
     q.table_cap = (int64_t)1 << lf;
-    q.hist_rows = lm > 0 ? ((int64_t)1 << (lm - 1)) : 0;
+    // every global level but the first gets its histograms from the level
+    // above (round-robin rule, k >= 2): one row per subtree of the deepest
+    q.hist_rows = lf > 0 ? ((int64_t)1 << (lf - 1)) : 0;
     q.sel_cap = lf > 0 ? ((int64_t)1 << (lf - 1)) : 0;
     size_t off = 0;
     q.off_status = off;

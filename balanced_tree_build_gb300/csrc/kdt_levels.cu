@@ -118,6 +118,7 @@ struct LevelArgs {
     uint32_t *hist_cur;  // [subtrees][kBuckets] (multi-CTA levels)
     uint32_t *hist_nxt;  // children's histograms (fused next level) or null
     SegSel *sel;
+    int hist_in;         // per-subtree levels: this level's histograms were built by the level above
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
     int64_t ld;          // records per group column
@@ -629,9 +630,15 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
 
 // ---- one CTA per subtree -------------------------------------------------------
 
+// One CTA per subtree: histogram (built by the level above when it could,
+// else from the split words), pick, partition, exact resolve.  With a fused
+// next level the children's histograms are built in shared memory during
+// the partition and written out whole (this CTA owns both rows); the
+// resolve then adds the candidates' contributions.
 __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a) {
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
+    __shared__ uint32_t fh[2 * kBuckets];
     __shared__ uint32_t red[64];
     __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t cursors[3];
@@ -644,12 +651,23 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     const SegInfo g = seg_info(a, s);
     const Bucketer bk = seg_bucketer(a, g.j, g.d);
     const int64_t ld = a.ld;
-    const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
-    for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
+    const bool fuse = a.hist_nxt != nullptr;
+    const int dn = (a.l + 1) % a.k;
+    if (a.hist_in) {
+        const uint32_t *H = a.hist_cur + g.j * kBuckets;
+        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = H[b];
+    } else {
+        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
+    }
+    if (fuse)
+        for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
     if (threadIdx.x < 3) cursors[threadIdx.x] = 0u;
     __syncthreads();
-    hist_range(col, g.base, g.base + (int64_t)g.n, bk, hist);
-    __syncthreads();
+    if (!a.hist_in) {
+        const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
+        hist_range(col, g.base, g.base + (int64_t)g.n, bk, hist);
+        __syncthreads();
+    }
     const bool ok = pick_bucket(hist, g.n, g.m, red, &pps);
     if (!ok) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
@@ -659,19 +677,26 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     if (threadIdx.x == 0) pps.klo = first_key_at_least(bk, pps.bstar);
     __syncthreads();
     const PartPlan pp = part_plan(g, pps.bstar, pps.below, pps.cnt, pps.klo, pps.khi);
-    Bucketer none;
-    none.lo = 0.f;
-    none.scale = 0.f;
+    Bucketer bkc;
+    bkc.lo = 0.f;
+    bkc.scale = 0.f;
+    if (fuse) bkc = seg_bucketer(a, g.j, dn);  // the children's: the parent's domain in dn
     for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile) {
         if (t0 + 2 * kTile < g.base + (int64_t)g.n) prefetch_tile(a, t0 + 2 * kTile, g.base + (int64_t)g.n);
-        part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, nullptr, none, 0);
+        part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, fuse ? fh : nullptr, bkc,
+                  dn);
     }
     __syncthreads();
     if (cursors[0] != pp.below || cursors[1] != pp.cnt || cursors[2] != pp.above) {
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    resolve_segment(a, g, pp, st, hist, red, medw, cur2, false, 0);
+    if (fuse) {
+        uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
+        for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) H[b] = fh[b];
+        __syncthreads();  // before the resolve adds the candidates to the same rows
+    }
+    resolve_segment(a, g, pp, st, hist, red, medw, cur2, fuse, dn);
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -695,6 +720,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.dim_nxt = b.dim[(l + 1) & 1];
     a.hist_cur = b.hist[l & 1];
     a.hist_nxt = nullptr;
+    a.hist_in = 0;
     a.sel = b.sel;
     a.status = b.status;
     a.per_cta = 0;
@@ -712,7 +738,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         a.per_cta = (live + grid - 1) / grid;
         const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
         const bool fused_here = l > 0 && fusable;
-        if (l + 1 < p.multi_levels && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
+        if (l + 1 < p.finish_level && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
         if (!fused_here) {
             if (cudaMemsetAsync(a.hist_cur, 0, (size_t)nseg * kBuckets * 4, stream) != cudaSuccess) return KDT_ECUDA;
             ProfScope ps(stream, "hist", 0.0);
@@ -735,6 +761,9 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
     } else {
+        // the level above built this level's histograms if it could
+        a.hist_in = fusable && l > 0 ? 1 : 0;
+        if (l + 1 < p.finish_level && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
         ProfScope ps(stream, "seg", alg);
         level_seg_kernel<<<(unsigned)nseg, kPartThreads, 0, stream>>>(a);
         if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
