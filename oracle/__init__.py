@@ -4,7 +4,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference leg may import this package.  The CUDA library never imports it and
 shares no code with it.  Every tree routine here is a thin ctypes wrapper
 around ``kdt_oracle.c``; see that file's header for the passages each routine
-follows.  ``gather_points`` (the points in level order) is its definition
+follows (the left-balanced tree, and the balanced median-split tree of
+Brown's presort-and-partition builder).  ``gather_points`` (the points in level order) is its definition
 written out with numpy indexing.
 """
 from __future__ import annotations
@@ -82,6 +83,14 @@ class Oracle:
         L.kdo_dist2.restype = ctypes.c_float
         L.kdo_knn_brute.argtypes = [f32p, i64, i32, f32p, i64, i32, f32p, f32p]
         L.kdo_knn_brute.restype = i32
+        L.kdo_balanced_slots.argtypes = [i64]
+        L.kdo_balanced_slots.restype = i64
+        L.kdo_build_balanced.argtypes = [f32p, i64, i32, f32p, i64]
+        L.kdo_build_balanced.restype = i32
+        L.kdo_verify_balanced.argtypes = [f32p, i64, i32, f32p, i64, ctypes.POINTER(ctypes.c_int64)]
+        L.kdo_verify_balanced.restype = i32
+        L.kdo_brute_force_balanced.argtypes = [f32p, i32, i32, f32p]
+        L.kdo_brute_force_balanced.restype = i64
 
     # -- notation ---------------------------------------------------------
     def level(self, i: int) -> int:
@@ -172,6 +181,45 @@ class Oracle:
         n, k = pts.shape
         first = np.full(n, -1, dtype=np.int32)
         cnt = self.lib.kdo_brute_force(pts.ctypes.data, n, k, mode, first.ctypes.data)
+        if cnt < 0:
+            raise OracleError(int(cnt))
+        return int(cnt), first
+
+
+    # -- the balanced (median-split) tree of Brown's builder ----------------
+    def balanced_slots(self, n: int) -> int:
+        """Heap slots of the balanced tree of n points: 2^numLevels(n) - 1."""
+        return int(self.lib.kdo_balanced_slots(n))
+
+    def build_balanced(self, pts: np.ndarray) -> np.ndarray:
+        """slots[s] = input index at heap slot s, -1 where a subtree is empty."""
+        pts = _points(pts)
+        n, k = pts.shape
+        slots = np.empty(self.balanced_slots(n), dtype=np.int32)
+        rc = self.lib.kdo_build_balanced(pts.ctypes.data, n, k, slots.ctypes.data, slots.size)
+        if rc != OK:
+            raise OracleError(rc)
+        return slots
+
+    def verify_balanced(self, pts: np.ndarray, slots: np.ndarray):
+        """Returns (ok, bad_slot): shape, permutation and the k-d condition of
+        every node against every ancestor (bad_slot -1: shape or permutation)."""
+        pts = _points(pts)
+        n, k = pts.shape
+        slots = np.ascontiguousarray(slots, dtype=np.int32)
+        bad = ctypes.c_int64(-2)
+        rc = self.lib.kdo_verify_balanced(pts.ctypes.data, n, k, slots.ctypes.data, slots.size,
+                                          ctypes.byref(bad))
+        if rc < 0:
+            raise OracleError(rc)
+        return rc == 0, int(bad.value)
+
+    def brute_force_balanced(self, pts: np.ndarray):
+        """Returns (number of valid assignments, first valid slot array)."""
+        pts = _points(pts)
+        n, k = pts.shape
+        first = np.full(self.balanced_slots(n), -1, dtype=np.int32)
+        cnt = self.lib.kdo_brute_force_balanced(pts.ctypes.data, n, k, first.ctypes.data)
         if cnt < 0:
             raise OracleError(int(cnt))
         return int(cnt), first

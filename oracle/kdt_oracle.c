@@ -25,6 +25,9 @@
  *   [B]  "Bigger Buffer k-d Trees on Multi-Many-Core Systems", nearest
  *        neighbour problem statement (K nearest reference points of a query
  *        in Euclidean distance) -- for the query routines at the end.
+ *   [R] again, overview list and build section, for the balanced
+ *        (median-split, not left-balanced) tree of Brown's presort-and-
+ *        partition builder: the kdo_*_balanced routines.
  *
  * Readings taken where the pages are silent:
  *   - the super key is cyclic from the split dimension p: (x[p], x[p+1 mod k],
@@ -400,6 +403,244 @@ int64_t kdo_brute_force(const float *pts, int N, int k, int mode,
         }
         /* next permutation (Heap's algorithm, iterative form) */
         int i = 1;
+        while (i < N && c[i] >= i) {
+            c[i] = 0;
+            i++;
+        }
+        if (i >= N)
+            break;
+        int j = (i % 2 == 0) ? 0 : c[i];
+        int32_t tmp = a[j];
+        a[j] = a[i];
+        a[i] = tmp;
+        c[i]++;
+    }
+    return valid;
+}
+
+/* ---- the balanced tree of [R] (Brown's presort-and-partition builder) ------
+ *
+ * [R] overview list: sort one reference array per coordinate; take the median
+ * of the first coordinate's array as the first node and partition the other
+ * arrays into the points below and above it (the median goes to neither
+ * side); repeat on both sides with the next coordinate, cycling through the
+ * coordinates, until every point is a node.  [R] build section: the medians
+ * of level L form a per-level store in which the children of entry j are
+ * entries 2j and 2j+1 of level L+1 -- heap order.
+ *
+ * Readings where the page is silent: the median of n points is the element of
+ * 0-based rank floor((n-1)/2) (the lower median); the order is the strict
+ * super key + index order above, so duplicates are kept and the tree is
+ * unique; the tree is stored in heap order, entry j of level L in slot
+ * 2^L - 1 + j of an array of 2^numLevels(N) - 1 slots, -1 where a subtree is
+ * empty.  The height is numLevels(N): the larger side of n points has
+ * floor(n/2).
+ *
+ * The builder is the definition written out: sort the subtree's points under
+ * its split order (level mod k), place the lower median, recurse. */
+
+/* Slots of the heap-ordered balanced tree of N points: 2^numLevels(N) - 1. */
+int64_t kdo_balanced_slots(int64_t N)
+{
+    if (N < 1 || N > INT32_MAX)
+        return -1;
+    return ((int64_t)1 << kdo_num_levels(N)) - 1;
+}
+
+static void rec_balanced(const float *pts, int k, int64_t slot, int level,
+                         int32_t *P, int64_t n, int32_t *slots, int64_t nslots,
+                         int *bad)
+{
+    if (n == 0)
+        return;
+    if (slot >= nslots) {
+        *bad = 1;
+        return;
+    }
+    g_pts = pts;
+    g_k = k;
+#if KDO_MUTANT == 7
+    g_p = (level + 1) % k; /* mutant: wrong round-robin phase */
+#else
+    g_p = level % k;
+#endif
+    qsort(P, (size_t)n, sizeof(int32_t), cmp_idx);
+#if KDO_MUTANT == 8
+    int64_t m = n / 2; /* mutant: upper median */
+#else
+    int64_t m = (n - 1) / 2;
+#endif
+    slots[slot] = P[m];
+#if KDO_MUTANT == 9
+    rec_balanced(pts, k, 2 * slot + 2, level + 1, P, m, slots, nslots, bad); /* mutant: sides swapped */
+    rec_balanced(pts, k, 2 * slot + 1, level + 1, P + m + 1, n - 1 - m, slots, nslots, bad);
+#else
+    rec_balanced(pts, k, 2 * slot + 1, level + 1, P, m, slots, nslots, bad);
+    rec_balanced(pts, k, 2 * slot + 2, level + 1, P + m + 1, n - 1 - m, slots, nslots, bad);
+#endif
+}
+
+/* slots[s] = input index of the point at heap slot s, -1 for an empty slot;
+ * nslots must be kdo_balanced_slots(N). */
+int kdo_build_balanced(const float *pts, int64_t N, int k, int32_t *slots, int64_t nslots)
+{
+    int rc = check_args(pts, N, k, 0);
+    if (rc != KDO_OK)
+        return rc;
+    if (!slots || nslots != kdo_balanced_slots(N))
+        return KDO_EINVAL;
+    int32_t *P = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+    if (!P)
+        return KDO_ENOMEM;
+    for (int64_t i = 0; i < N; i++)
+        P[i] = (int32_t)i;
+    for (int64_t s = 0; s < nslots; s++)
+        slots[s] = -1;
+    int bad = 0;
+    rec_balanced(pts, k, 0, 0, P, N, slots, nslots, &bad);
+    free(P);
+    return bad ? KDO_EINTERNAL : KDO_OK;
+}
+
+/* Shape of the balanced tree: occ[s] = 1 if slot s holds a point.  Sizes
+ * follow the split rule (left floor((n-1)/2), right n-1-left), computed by an
+ * explicit stack (no sorting involved). */
+static int balanced_shape(int64_t N, uint8_t *occ, int64_t nslots)
+{
+    typedef struct { int64_t slot, n; } item;
+    item *st = (item *)malloc(sizeof(item) * 128);
+    if (!st)
+        return KDO_ENOMEM;
+    int sp = 0;
+    memset(occ, 0, (size_t)nslots);
+    st[sp++] = (item){0, N};
+    while (sp > 0) {
+        item it = st[--sp];
+        if (it.n == 0)
+            continue;
+        if (it.slot >= nslots || sp + 2 > 128) {
+            free(st);
+            return KDO_EINTERNAL;
+        }
+        occ[it.slot] = 1;
+        int64_t m = (it.n - 1) / 2;
+        st[sp++] = (item){2 * it.slot + 1, m};
+        st[sp++] = (item){2 * it.slot + 2, it.n - 1 - m};
+    }
+    free(st);
+    return KDO_OK;
+}
+
+/* Node s (occupied) against each of its ancestors a, split dimension
+ * level(a) mod k: the strict order puts it below a if it lies in a's left
+ * subtree, above a otherwise. */
+static int balanced_node_ok(const float *pts, int64_t N, int k, const int32_t *slots, int64_t s)
+{
+    int depth = kdo_level(s);
+    int64_t a = 0;
+    for (int j = 0; j < depth; j++) {
+        int right = (int)(((uint64_t)(s + 1) >> (depth - 1 - j)) & 1u);
+        int d = kdo_level(a) % k;
+        int64_t pa = slots[a], ps = slots[s];
+        if (pa < 0 || pa >= N || ps < 0 || ps >= N)
+            return 0;
+        if (right ? !kdo_less(pts, k, d, pa, ps) : !kdo_less(pts, k, d, ps, pa))
+            return 0;
+        a = 2 * a + 1 + right;
+    }
+    return 1;
+}
+
+/* Checks that slots holds exactly the shape of the balanced tree of N points
+ * (occupied slots as the split rule gives them, -1 elsewhere), that the
+ * occupied slots hold a permutation of 0..N-1, and the k-d condition of every
+ * node against every ancestor.  By uniqueness, valid == equal to
+ * kdo_build_balanced.  Returns 0 if valid, 1 if not (first failing slot in
+ * *bad_slot, -1 for a shape or permutation failure), <0 on error. */
+int kdo_verify_balanced(const float *pts, int64_t N, int k, const int32_t *slots,
+                        int64_t nslots, int64_t *bad_slot)
+{
+    int rc = check_args(pts, N, k, 0);
+    if (rc != KDO_OK)
+        return rc;
+    if (!slots || nslots != kdo_balanced_slots(N))
+        return KDO_EINVAL;
+    uint8_t *occ = (uint8_t *)malloc((size_t)nslots);
+    uint8_t *seen = (uint8_t *)calloc((size_t)N, 1);
+    if (!occ || !seen) {
+        free(occ);
+        free(seen);
+        return KDO_ENOMEM;
+    }
+    rc = balanced_shape(N, occ, nslots);
+    int result = 0;
+    if (bad_slot)
+        *bad_slot = -1;
+    for (int64_t s = 0; rc == KDO_OK && s < nslots && result == 0; s++) {
+        int32_t v = slots[s];
+        if (!occ[s]) {
+            if (v != -1)
+                result = 1;
+            continue;
+        }
+        if (v < 0 || v >= N || seen[v])
+            result = 1;
+        else
+            seen[v] = 1;
+    }
+    for (int64_t s = 0; rc == KDO_OK && s < nslots && result == 0; s++) {
+        if (occ[s] && !balanced_node_ok(pts, N, k, slots, s)) {
+            result = 1;
+            if (bad_slot)
+                *bad_slot = s;
+        }
+    }
+    free(occ);
+    free(seen);
+    return rc != KDO_OK ? rc : result;
+}
+
+/* Exhaustive search: every assignment of the N points to the occupied slots
+ * (Heap's algorithm over the occupied slots in heap order); counts the
+ * assignments that satisfy the k-d condition and stores the first one
+ * (N <= 11). */
+int64_t kdo_brute_force_balanced(const float *pts, int N, int k, int32_t *first_valid)
+{
+    if (check_args(pts, N, k, 0) != KDO_OK || N > 11)
+        return -1;
+    int64_t nslots = kdo_balanced_slots(N);
+    uint8_t occ[2048];
+    int64_t where[11];
+    if (nslots > 2048 || balanced_shape(N, occ, nslots) != KDO_OK)
+        return -1;
+    int cnt = 0;
+    for (int64_t s = 0; s < nslots; s++)
+        if (occ[s])
+            where[cnt++] = s;
+    if (cnt != N)
+        return -1;
+    int32_t slots[2048];
+    int32_t a[11];
+    int c[11];
+    for (int i = 0; i < N; i++) {
+        a[i] = i;
+        c[i] = 0;
+    }
+    int64_t valid = 0;
+    for (;;) {
+        for (int64_t s = 0; s < nslots; s++)
+            slots[s] = -1;
+        for (int i = 0; i < N; i++)
+            slots[where[i]] = a[i];
+        int ok = 1;
+        for (int i = 0; i < N && ok; i++)
+            ok = balanced_node_ok(pts, N, k, slots, where[i]);
+        if (ok) {
+            if (valid == 0 && first_valid)
+                memcpy(first_valid, slots, sizeof(int32_t) * (size_t)nslots);
+            valid++;
+        }
+        int i = 1; /* next permutation (Heap's algorithm, iterative form) */
         while (i < N && c[i] >= i) {
             c[i] = 0;
             i++;

@@ -8,7 +8,8 @@ planted mutants (each must fail at least one pin).
 Sources: "GPU-friendly, Parallel, and (Almost-)In-Place Construction of
 Left-Balanced k-d Trees" (problem, notation, round-robin, widest-dimension and
 worked-example passages); "An Implementation of a Balanced Kd Tree Builder
-Using GPUs" (super-key comparison).
+Using GPUs" (super-key comparison; overview list and build section for the
+balanced tree of Brown's builder).
 """
 from __future__ import annotations
 
@@ -239,6 +240,102 @@ def pin_verifier_rejects(o):
         assert not ok and node == -1
 
 
+# ---------------------------------------------------------------------------
+# the balanced (median-split) tree of Brown's builder: "An Implementation of
+# a Balanced Kd Tree Builder Using GPUs", overview list (sort, take the
+# median, partition the other arrays, cycle through the coordinates) and
+# build section (per-level median store, children of entry j at 2j, 2j+1).
+
+def balanced_shape_by_sizes(n: int) -> set:
+    """Occupied heap slots of the balanced tree of n points, from the split
+    rule alone: the lower side gets floor((m-1)/2) of a subtree's m points."""
+    occ, stack = set(), [(0, n)]
+    while stack:
+        s, m = stack.pop()
+        if m == 0:
+            continue
+        occ.add(s)
+        left = (m - 1) // 2
+        stack += [(2 * s + 1, left), (2 * s + 2, m - 1 - left)]
+    return occ
+
+
+def heap_inorder(slots: np.ndarray) -> list:
+    """Occupied slots' values in in-order (left subtree, node, right subtree)."""
+    out, stack, s = [], [], 0
+    while stack or (s < slots.size and slots[s] >= 0):
+        while s < slots.size and slots[s] >= 0:
+            stack.append(s)
+            s = 2 * s + 1
+        s = stack.pop()
+        out.append(int(slots[s]))
+        s = 2 * s + 2
+    return out
+
+
+def lexsort_super(pts: np.ndarray, ids: np.ndarray, p: int) -> np.ndarray:
+    """ids ordered by (x[p], x[p+1 mod k], ..., input index) with numpy's
+    lexsort on explicit key columns (the last key is the primary one)."""
+    k = pts.shape[1]
+    keys = [ids] + [pts[ids, (p + j) % k] for j in reversed(range(k))]
+    return ids[np.lexsort(keys)]
+
+
+def pin_balanced_brute_force_unique(o, sizes=range(1, 9), ks=(1, 2, 3)):
+    for n in sizes:
+        for k in ks:
+            for dist in ("uniform01", "dup_heavy", "all_equal", "int_grid"):
+                pts = make_points(dist, n, k, seed=100 * n + k)
+                cnt, first = o.brute_force_balanced(pts)
+                assert cnt == 1, (n, k, dist, cnt)
+                assert np.array_equal(o.build_balanced(pts), first), (n, k, dist)
+
+
+def pin_balanced_shape(o):
+    for n in list(range(1, 130)) + [1000, 4095, 4096, 4097, 65537]:
+        pts = make_points("uniform01", n, 2, seed=n)
+        slots = o.build_balanced(pts)
+        assert slots.size == 2 ** n.bit_length() - 1
+        assert set(np.nonzero(slots >= 0)[0].tolist()) == balanced_shape_by_sizes(n), n
+        assert np.array_equal(np.sort(slots[slots >= 0]), np.arange(n))
+
+
+def pin_balanced_k1_inorder_sorted(o):
+    for n in (1, 2, 3, 10, 31, 32, 100, 1000):
+        for dist in ("uniform01", "dup_heavy"):
+            pts = make_points(dist, n, 1, seed=n + 7)
+            want = lexsort_super(pts, np.arange(n), 0)
+            assert heap_inorder(o.build_balanced(pts)) == want.tolist(), (n, dist)
+
+
+def pin_balanced_root_and_children(o):
+    for n, dist, k in [(101, "dup_heavy", 3), (1000, "uniform01", 2), (64, "int_grid", 3), (7, "all_equal", 2)]:
+        pts = make_points(dist, n, k, seed=n)
+        slots = o.build_balanced(pts)
+        order0 = lexsort_super(pts, np.arange(n), 0)
+        m = (n - 1) // 2
+        assert slots[0] == order0[m], (n, dist)
+        for part, slot in ((order0[:m], 1), (order0[m + 1:], 2)):
+            if part.size == 0:
+                continue
+            o1 = lexsort_super(pts, np.sort(part), 1 % k)
+            assert slots[slot] == o1[(part.size - 1) // 2], (n, dist, slot)
+
+
+def pin_balanced_verifier_rejects(o):
+    pts = make_points("dup_heavy", 300, 3, seed=3)
+    slots = o.build_balanced(pts)
+    assert o.verify_balanced(pts, slots)[0]
+    occ = np.nonzero(slots >= 0)[0]
+    bad = slots.copy()
+    bad[[occ[5], occ[200]]] = bad[[occ[200], occ[5]]]
+    assert not o.verify_balanced(pts, bad)[0]
+    moved = slots.copy()
+    hole = int(np.nonzero(slots < 0)[0][0])
+    moved[hole], moved[occ[-1]] = moved[occ[-1]], -1
+    assert not o.verify_balanced(pts, moved)[0]
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_less_is_tuple_order,
@@ -251,4 +348,9 @@ ALL_PINS = [
     pin_cyclic_tiebreak_top_nodes,
     pin_widest_root_and_children,
     pin_verifier_rejects,
+    pin_balanced_brute_force_unique,
+    pin_balanced_shape,
+    pin_balanced_k1_inorder_sorted,
+    pin_balanced_root_and_children,
+    pin_balanced_verifier_rejects,
 ]

@@ -15,6 +15,8 @@ MUTANTS = {
     5: "left and right subtrees swapped",
     6: "left child domain clipped on the wrong side",
     7: "round-robin phase shifted by one level",
+    8: "balanced tree: upper median instead of lower",
+    9: "balanced tree: subtrees swapped",
 }
 
 

@@ -22,6 +22,14 @@ def test_brute_force_n10_worked_example_unique(o):
     assert (o.build_tree(pts, mode=1) == first).all()
 
 
+def test_balanced_brute_force_n10_unique(o):
+    pts, _, _ = _pins.load_worked_example()
+    for p in (pts, pts[:, ::-1].copy()):
+        cnt, first = o.brute_force_balanced(p)
+        assert cnt == 1
+        assert (o.build_balanced(p) == first).all()
+
+
 def test_oracle_rejects_bad_input(o):
     import numpy as np
     pts = np.zeros((4, 2), dtype=np.float32)

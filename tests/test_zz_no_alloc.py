@@ -5,8 +5,8 @@ whose host application owns all device memory, a latency-critical loop where
 an allocation could stall or fail) use kdt_build_static, which takes its
 scratch from one fixed array that the library reserves on each device.  These
 tests call it through the C ABI twice in a row and compare its output with
-the regular entry point kdt_build_ws (exact equality: the tree is unique, so
-the permutations must match element for element).
+the CPU oracle and with the regular entry point kdt_build_ws (exact equality:
+the tree is unique, so the permutations must match element for element).
 
 This file is named so that pytest collects it last.
 """
@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import balanced_tree_build_gb300 as kdt
+import oracle
 from balanced_tree_build_gb300.inputs import make_points
 from gpu_util import ensure_library
 
@@ -75,6 +76,9 @@ def test_matches_regular_entry_point_twice(dist, n, k, mode):
     b = torch.from_numpy(make_points(dist, n, k, seed=42)).cuda()
     first = _build_static(fn, a, mode)
     second = _build_static(fn, b, mode)  # reuses the array left dirty by the first call
+    o = oracle.get()
+    assert np.array_equal(first, o.build_tree(a.cpu().numpy(), mode))
+    assert np.array_equal(second, o.build_tree(b.cpu().numpy(), mode))
     assert np.array_equal(first, _build_ws(a, mode))
     assert np.array_equal(second, _build_ws(b, mode))
 
@@ -84,7 +88,9 @@ def test_smaller_build_after_larger_one():
     big = torch.from_numpy(make_points("uniform01", 400_000, 3, seed=7)).cuda()
     small = torch.from_numpy(make_points("gaussian", 777, 3, seed=8)).cuda()
     _build_static(fn, big, 0)
-    assert np.array_equal(_build_static(fn, small, 0), _build_ws(small, 0))
+    got = _build_static(fn, small, 0)
+    assert np.array_equal(got, oracle.get().build_tree(small.cpu().numpy(), 0))
+    assert np.array_equal(got, _build_ws(small, 0))
 
 
 def test_rejects_builds_that_do_not_fit():
