@@ -67,6 +67,9 @@ def _load():
     L.kdt_build_inplace.argtypes = [vp, i64, i32, i32, vp, vp, sz, vp]
     L.kdt_node_dims.argtypes = [vp, i64, i32, i32, vp, vp]
     L.kdt_knn.argtypes = [vp, i64, i32, vp, vp, i64, i32, vp, vp, vp]
+    L.kdt_balanced_slots.argtypes = [i64, ctypes.POINTER(i64)]
+    L.kdt_balanced_workspace_size.argtypes = [i64, i32, ctypes.POINTER(sz)]
+    L.kdt_build_balanced.argtypes = [vp, i64, i32, vp, vp, sz, vp]
     L.kdt_status.argtypes = [vp]
     L.kdt_error_string.argtypes = [i32]
     L.kdt_error_string.restype = ctypes.c_char_p
@@ -74,7 +77,8 @@ def _load():
     L.kdt_profile_read.argtypes = [ctypes.POINTER(_KernelStat), i32]
     for name in ("kdt_workspace_size", "kdt_host_workspace_size", "kdt_build", "kdt_build_ws",
                  "kdt_build_host", "kdt_verify", "kdt_gather_points", "kdt_build_inplace", "kdt_node_dims",
-                 "kdt_knn", "kdt_status",
+                 "kdt_knn", "kdt_status", "kdt_balanced_slots", "kdt_balanced_workspace_size",
+                 "kdt_build_balanced",
                  "kdt_profile_enable",
                  "kdt_profile_reset", "kdt_profile_read"):
         getattr(L, name).restype = i32
@@ -194,6 +198,40 @@ def build_tree_host(points, mode: int = SPLIT_ROUND_ROBIN, out=None, workspace=N
                                 workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     del keep
     _check(rc, "kdt_build_host")
+    return out
+
+
+def balanced_slots(n: int) -> int:
+    """Heap slots of the balanced (median-split) tree of n points."""
+    out = ctypes.c_int64(0)
+    _check(_load().kdt_balanced_slots(n, ctypes.byref(out)), "kdt_balanced_slots")
+    return int(out.value)
+
+
+def balanced_workspace_bytes(n: int, k: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_load().kdt_balanced_workspace_size(n, k, ctypes.byref(out)), "kdt_balanced_workspace_size")
+    return int(out.value)
+
+
+def build_balanced(points, out=None, workspace=None, stream=None):
+    """Builds the balanced tree of Brown's builder (lower median, split
+    dimension level mod k) over ``points`` (CUDA float32 [N, k]); returns int32
+    [balanced_slots(N)] in heap order, -1 in the slots of empty subtrees.
+    Stream-ordered."""
+    import torch
+    n, k = _check_points(points)
+    slots = balanced_slots(n)
+    if out is None:
+        out = torch.empty(slots, dtype=torch.int32, device=points.device)
+    elif out.dtype != torch.int32 or out.shape != (slots,) or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA int32 tensor of shape (balanced_slots(N),)")
+    if workspace is None:
+        workspace = torch.empty(balanced_workspace_bytes(n, k), dtype=torch.uint8, device=points.device)
+    rc = _load().kdt_build_balanced(ctypes.c_void_p(points.data_ptr()), n, k, ctypes.c_void_p(out.data_ptr()),
+                                    ctypes.c_void_p(workspace.data_ptr()),
+                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(rc, "kdt_build_balanced")
     return out
 
 

@@ -152,6 +152,32 @@ int kdt_build(const float *pts, int64_t N, int k, int split_mode, int32_t *perm,
     return rc;
 }
 
+int kdt_balanced_slots(int64_t N, int64_t *slots) {
+    if (!slots || N < 1 || N > 2147483647LL) return KDT_EINVAL;
+    *slots = ((int64_t)1 << make_shape(N).L) - 1;
+    return KDT_OK;
+}
+
+int kdt_balanced_workspace_size(int64_t N, int k, size_t *bytes) {
+    if (!bytes) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, KDT_SPLIT_ROUND_ROBIN, &p, kShapeBalanced);
+    if (rc != KDT_OK) return rc;
+    *bytes = p.bytes;
+    return KDT_OK;
+}
+
+int kdt_build_balanced(const float *pts, int64_t N, int k, int32_t *slots, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    if (!pts || !slots || !workspace) return KDT_EINVAL;
+    Plan p;
+    const int rc = make_plan(N, k, KDT_SPLIT_ROUND_ROBIN, &p, kShapeBalanced);
+    if (rc != KDT_OK) return rc;
+    if (workspace_bytes < p.bytes) return KDT_ENOMEM;
+    if (!aligned256(workspace)) return KDT_EINVAL;
+    return enqueue_build(p, carve(p, workspace), pts, slots, static_cast<cudaStream_t>(stream));
+}
+
 int kdt_host_workspace_size(int64_t N, int k, int split_mode, size_t *bytes) {
     if (!bytes) return KDT_EINVAL;
     Plan p;

@@ -148,15 +148,16 @@ __global__ void root_table_kernel(const uint32_t *bbox, int k, float *dom, int *
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int make_plan(int64_t N, int k, int mode, Plan *p) {
+int make_plan(int64_t N, int k, int mode, Plan *p, int shape) {
     if (N < 1 || N > 2147483647LL || k < 1 || k > kMaxK || (mode != 0 && mode != 1)) return KDT_EINVAL;
+    if (shape != kShapeLeftBalanced && (shape != kShapeBalanced || mode != KDT_SPLIT_ROUND_ROBIN)) return KDT_EINVAL;
     Plan q{};
-    q.S = make_shape(N);
+    q.S = make_shape(N, shape);
     q.k = k;
     q.mode = mode;
     if (pick_tile(k, mode, &q.tp) != 0) return KDT_EINVAL;
     int lf = 0;
-    while (lf < q.S.L && seg_size(q.S, lf, full_nodes(lf)) > q.tp.tile) ++lf;
+    while (lf < q.S.L && largest_subtree(q.S, lf) > q.tp.tile) ++lf;
     q.finish_level = lf;
     int lm = 0;
     // every level with few subtrees runs on the whole GPU (multi-CTA); the
@@ -223,6 +224,10 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
     const int k = p.k;
     const double Nd = (double)S.N;
     if (cudaMemsetAsync(b.status, 0, sizeof(int), stream) != cudaSuccess) return KDT_ECUDA;
+    if (S.kind == kShapeBalanced) {  // heap slots of empty subtrees read -1
+        const size_t slots = (((size_t)1) << S.L) - 1;
+        if (cudaMemsetAsync(perm, 0xff, slots * sizeof(int32_t), stream) != cudaSuccess) return KDT_ECUDA;
+    }
     if (cudaMemsetAsync(b.bbox, 0xff, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
     if (cudaMemsetAsync(b.bbox + k, 0x00, (size_t)k * 4, stream) != cudaSuccess) return KDT_ECUDA;
     {

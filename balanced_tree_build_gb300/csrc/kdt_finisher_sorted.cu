@@ -160,6 +160,72 @@ __device__ __forceinline__ uint32_t io_lo(uint32_t i, int l, int h, uint32_t Mt)
     return P < 2u * Mt ? P : (P >> 1) + Mt;
 }
 
+// The same maps for a tile of the balanced shape (n points): walks over the
+// gap ranges of its nodes (see bal_node).  An empty node's "position" is its
+// gap start; no point is ever assigned to it.
+__device__ __forceinline__ uint32_t tile_node1(bool bal, uint32_t p, int h, uint32_t Mt, uint32_t n) {
+    if (!bal) return io_node1(p, h, Mt);
+    uint32_t u = 1u, a = 0u, c = n + 1u;
+    for (int t = 0; t < 32; ++t) {
+        const uint32_t hh = c >> 1;
+        if (hh == 0u) return 0u;  // not inside any node: cannot happen for p < n
+        const uint32_t pos = a + hh - 1u;
+        if (p == pos) return u;
+        if (p < pos) {
+            c = hh;
+            u = 2u * u;
+        } else {
+            a += hh;
+            c -= hh;
+            u = 2u * u + 1u;
+        }
+    }
+    return 0u;
+}
+
+__device__ __forceinline__ uint32_t tile_pos(bool bal, uint32_t i, int l, int h, uint32_t Mt, uint32_t n) {
+    if (!bal) return io_pos(i, l, h, Mt);
+    int64_t g0, m;
+    bal_node(n, l, i, &g0, &m);
+    return (uint32_t)(m >= 2 ? g0 + (m >> 1) - 1 : g0);
+}
+
+__device__ __forceinline__ uint32_t tile_lo(bool bal, uint32_t i, int l, int h, uint32_t Mt, uint32_t n) {
+    if (!bal) return io_lo(i, l, h, Mt);
+    int64_t g0, m;
+    bal_node(n, l, i, &g0, &m);
+    return (uint32_t)g0;
+}
+
+// Orders arr[0, T) = the local ids 0..n-1 (padding ids >= n last) by the
+// super key of coordinate c: an in-place bitonic sort in shared memory, used
+// for a crowded coordinate of a balanced-shape tile (a value bucket with more
+// points than the counting sort ranks).  T is a power of two.
+template <int NT>
+__device__ void bitonic_sort_ids(uint16_t *arr, const uint32_t *kc, const uint32_t *keys, const uint32_t *idx, int T,
+                                 int k, int c, uint32_t n) {
+    for (uint32_t q = threadIdx.x; q < (uint32_t)T; q += NT) arr[q] = (uint16_t)q;
+    __syncthreads();
+    for (uint32_t size = 2; size <= (uint32_t)T; size <<= 1) {
+        for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (uint32_t t = threadIdx.x; t < (uint32_t)T / 2u; t += NT) {
+                const uint32_t i = 2u * t - (t & (stride - 1u)), j = i + stride;
+                const uint32_t x = arr[i], y = arr[j];
+                // y before x under the order (ids >= n after everything)?
+                bool y_first;
+                if (x >= n || y >= n) y_first = x >= n && (y < n || y < x);
+                else y_first = kc[y] < kc[x] || (kc[y] == kc[x] && sk_less_tail(keys, idx, T, k, c, y, x));
+                const bool up = (i & size) == 0u;
+                if (y_first == up) {
+                    arr[i] = (uint16_t)y;
+                    arr[j] = (uint16_t)x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 // Split dimension of tile node i on relative depth `depth` under the widest
 // rule: clip the tile root's domain by the splits of the node's ancestors
 // (recorded in sval / sdim), top-down.
@@ -240,6 +306,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     const int64_t s0 = full_nodes(a.l0) + tile;
     const uint32_t n = (uint32_t)seg_size(S, a.l0, s0);
     const int64_t base = seg_begin(S, a.l0, s0);
+    const bool bal = S.kind == kShapeBalanced;  // the tile's own shape: left-balanced or balanced
     if (n < 1u || n > (uint32_t)T || T != E * NT || nb != 2 * T) {
         if (tid == 0) {
             set_status(a.status, KDT_EINTERNAL);
@@ -291,6 +358,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
             spread = scale > 0.f && scale <= 3.0e38f;
         }
         if (!spread && n > (uint32_t)kSfMaxBucket) {  // same decision in every thread
+            if (bal) {  // balanced tiles have no select fallback: sort this coordinate outright
+                bitonic_sort_ids<NT>(sm.ids + c * T, kc, sm.keys, sm.idx, T, k, c, n);
+                continue;
+            }
             fail = true;
             break;
         }
@@ -314,6 +385,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
             }
         }
         if (__syncthreads_or(big)) {
+            if (bal) {
+                bitonic_sort_ids<NT>(sm.ids + c * T, kc, sm.keys, sm.idx, T, k, c, n);
+                continue;
+            }
             fail = true;
             break;
         }
@@ -403,10 +478,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     uint32_t g[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        const uint32_t u1 = p0 + e < n ? io_node1(p0 + e, h, Mt) : 0u;
+        const uint32_t u1 = p0 + e < n ? tile_node1(bal, p0 + e, h, Mt, n) : 0u;
         g[e] = u1 ? ((u1 << 1) | 1u) << (__clz((int)u1) - 1) : 0u;
     }
-    uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? io_node1(p0 - 1u, h, Mt) : 0u;
+    uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? tile_node1(bal, p0 - 1u, h, Mt, n) : 0u;
     gprev = gprev ? ((gprev << 1) | 1u) << (__clz((int)gprev) - 1) : 0u;
     const int last = h - 2;  // deepest level that moves an array
     if (!rr) {
@@ -428,14 +503,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         constexpr uint64_t kHead64 = 1ull << 63;
         uint32_t *side32 = sm.side;                                 // [T]: two 16-bit sides, by level parity
         uint16_t *side16 = reinterpret_cast<uint16_t *>(sm.side);
-        uint16_t *ptab0 = reinterpret_cast<uint16_t *>(sm.ntab);   // [T/2] in-order position of each node of a level
+        uint16_t *ptab0 = reinterpret_cast<uint16_t *>(sm.ntab);   // [T/2] in-order position + 1 of each node of a level
         uint16_t *ptab1 = ptab0 + T / 2;
         int dl = a.l0 % 3;
         for (int l = 0; l < last; ++l, dl = dl == 2 ? 0 : dl + 1) {
             const uint32_t q = (uint32_t)l & 1u;
             uint16_t *pt_l = q ? ptab1 : ptab0;
             const uint16_t *pt_p = q ? ptab0 : ptab1;  // level l - 1
-            for (uint32_t i = tid; i < (1u << l); i += NT) pt_l[i] = (uint16_t)io_pos(i, l, h, Mt);
+            for (uint32_t i = tid; i < (1u << l); i += NT) pt_l[i] = (uint16_t)(tile_pos(bal, i, l, h, Mt, n) + 1u);
             // A: side of every point of a level-l node, from d_l: 0 left,
             //    1 right, 0x8000 | position for the node's split point
             if (wact) {
@@ -466,11 +541,11 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                     if (lv && !pl) {  // first position of a level-(l-1) node w
                         uint64_t base = (uint64_t)(p0 + (uint32_t)e);
                         if (l == 0) {
-                            base |= (uint64_t)(pt_l[0] + 1u) << 16;
+                            base |= (uint64_t)pt_l[0] << 16;
                         } else {
                             const uint32_t wi = (g[e] >> (32 - l)) ^ (1u << (l - 1));
-                            base |= ((uint64_t)(pt_l[2u * wi] + 1u) << 16) | ((uint64_t)(pt_p[wi] + 1u) << 32) |
-                                    ((uint64_t)(pt_l[2u * wi + 1u] + 1u) << 48);
+                            base |= ((uint64_t)pt_l[2u * wi] << 16) | ((uint64_t)pt_p[wi] << 32) |
+                                    ((uint64_t)pt_l[2u * wi + 1u] << 48);
                         }
                         run = kHead64 | base;
                     }
@@ -549,7 +624,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                 if (mv == 0u) break;  // k >= 2: only for l >= h-2; k == 1: never moves
             }
             // this level's node ranges: lo | pos << 16 per node
-            for (uint32_t i = tid; i < (1u << l); i += NT) sm.ntab[i] = io_lo(i, l, h, Mt) | (io_pos(i, l, h, Mt) << 16);
+            for (uint32_t i = tid; i < (1u << l); i += NT)
+                sm.ntab[i] = tile_lo(bal, i, l, h, Mt, n) | (tile_pos(bal, i, l, h, Mt, n) << 16);
             // live / head masks: a node range starts at p if p is live and p-1
             // is not (p-1 holds a fixed ancestor, or p == 0)
             uint32_t live = 0u, head = 0u;
@@ -672,11 +748,17 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     //    pos(u) from an array that is final there -- in round-robin mode the
     //    array of its own level's split coordinate (leaves: the one of level
     //    h-2), in widest mode any (all arrays move on every level)
-    for (uint32_t u = tid; u < n; u += NT) {
+    const uint32_t nodes = bal ? (1u << h) - 1u : n;  // balanced: empty slots keep the -1 written up front
+    for (uint32_t u = tid; u < nodes; u += NT) {
         const uint32_t g1 = u + 1u;
         const int lv = 31 - __clz((int)g1);
         const uint32_t i = g1 - (1u << lv);
-        const uint32_t p = io_pos(i, lv, h, Mt);
+        if (bal) {
+            int64_t g0, m;
+            bal_node(n, lv, i, &g0, &m);
+            if (m < 2) continue;  // an empty subtree
+        }
+        const uint32_t p = tile_pos(bal, i, lv, h, Mt, n);
         if (p >= n) {
             set_status(a.status, KDT_EINTERNAL);
             continue;
@@ -748,7 +830,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     // subtrees of 2B-1 points, one of B-1+rem, the rest B-1.
     const int Ts = a.T / 2;
     int64_t nbig = ntiles;
-    if (Ts >= 512) {
+    if (Ts >= 512 && S.kind != kShapeBalanced) {
         const int lgB = S.L - 1 - p.finish_level;
         const int64_t B = (int64_t)1 << lgB, q = S.M >> lgB, rem = S.M - (q << lgB);
         if (B - 1 <= Ts) {
@@ -783,6 +865,7 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
             if (rc != KDT_OK) return rc;
         }
     }
+    if (S.kind == kShapeBalanced) return KDT_OK;  // balanced tiles never fall back (crowded coordinates are sorted)
     ProfScope ps(stream, "finisher_select", 0.0);
     return launch_select_finisher(p, b, src, perm, b.fallback, stream);
 }

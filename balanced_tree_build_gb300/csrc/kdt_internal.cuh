@@ -40,22 +40,63 @@ __host__ __device__ __forceinline__ int level_of(int64_t i) { return ilog2_u64((
 
 __host__ __device__ __forceinline__ int64_t full_nodes(int l) { return ((int64_t)1 << l) - 1; }
 
+// Tree shapes.  KDT_SHAPE_LEFT_BALANCED: the left-balanced complete tree of
+// the left-balanced paper (levels full but the last, which fills from the
+// left).  KDT_SHAPE_BALANCED: the median-split tree of Brown's builder ("An
+// Implementation of a Balanced Kd Tree Builder Using GPUs", overview list):
+// a node of n points keeps the point of rank floor((n-1)/2), so its lower
+// side has floor((n-1)/2) points and its upper side the rest; nodes are
+// numbered in heap order with empty slots where a subtree is empty.
+constexpr int kShapeLeftBalanced = 0, kShapeBalanced = 1;
+
 struct Shape {
-    int64_t N;  // number of points / nodes
-    int L;      // numLevels(N)
-    int64_t M;  // nodes on the last level
+    int64_t N;  // number of points
+    int L;      // numLevels(N): levels of either shape
+    int64_t M;  // left-balanced: nodes on the last level
+    int kind;   // kShapeLeftBalanced or kShapeBalanced
 };
 
-__host__ __device__ __forceinline__ Shape make_shape(int64_t N) {
+__host__ __device__ __forceinline__ Shape make_shape(int64_t N, int kind = kShapeLeftBalanced) {
     Shape S;
     S.N = N;
     S.L = level_of(N - 1) + 1;
     S.M = N - full_nodes(S.L - 1);
+    S.kind = kind;
     return S;
 }
 
+// Balanced shape of n points: node i of level l (heap order) covers the gaps
+// [g0, g0 + m) among the n + 1 gaps around its in-order positions -- its
+// points are the in-order positions [g0, g0 + m - 1) (none if m <= 1) and its
+// split point sits at g0 + floor(m/2) - 1.  The lower child gets floor(m/2)
+// of the gaps, the upper child the rest: a walk from the root, O(l).
+__host__ __device__ __forceinline__ void bal_node(int64_t n, int l, int64_t i, int64_t *g0, int64_t *m) {
+    int64_t a = 0, c = n + 1;
+    for (int t = l - 1; t >= 0; --t) {
+        const int64_t h = c >> 1;
+        if ((i >> t) & 1) {
+            a += h;
+            c -= h;
+        } else {
+            c = h;
+        }
+    }
+    *g0 = a;
+    *m = c;
+}
+
+// Largest subtree on level l (the splits of both shapes put at least as many
+// points on the side that the largest subtree descends into).
+__host__ __device__ __forceinline__ int64_t largest_subtree(const Shape &S, int l);
+
 // ss(s) for node s on level l (0 if the node does not exist).
 __host__ __device__ __forceinline__ int64_t seg_size(const Shape &S, int l, int64_t s) {
+    if (S.kind == kShapeBalanced) {
+        if (l >= S.L) return 0;
+        int64_t g0, m;
+        bal_node(S.N, l, s - full_nodes(l), &g0, &m);
+        return m > 1 ? m - 1 : 0;
+    }
     if (l >= S.L || s >= S.N) return 0;
     const int64_t B = (int64_t)1 << (S.L - 1 - l);
     const int64_t A = B - 1;
@@ -65,8 +106,18 @@ __host__ __device__ __forceinline__ int64_t seg_size(const Shape &S, int l, int6
     return A + r;
 }
 
-// sb(s, l) for node s on level l.
+// sb(s, l) for node s on level l: the first array position of subtree s when
+// the F(l) nodes above level l own positions 0..F(l)-1 and the live subtrees
+// follow in node order (balanced shape: on levels whose nodes all hold points,
+// where the i subtrees before node i are separated by i fixed positions in
+// the in-order numbering).
 __host__ __device__ __forceinline__ int64_t seg_begin(const Shape &S, int l, int64_t s) {
+    if (S.kind == kShapeBalanced) {
+        int64_t g0, m;
+        const int64_t i = s - full_nodes(l);
+        bal_node(S.N, l, i, &g0, &m);
+        return full_nodes(l) + g0 - i;
+    }
     const int64_t B = (int64_t)1 << (S.L - 1 - l);
     const int64_t A = B - 1;
     const int64_t j = s - full_nodes(l);
@@ -74,8 +125,15 @@ __host__ __device__ __forceinline__ int64_t seg_begin(const Shape &S, int l, int
     return full_nodes(l) + j * A + (t < S.M ? t : S.M);
 }
 
-// 32-bit forms of ss and sb for device code: with N < 2^31 every node id,
-// size and position fits; requires l < L and s on level l.
+__host__ __device__ __forceinline__ int64_t largest_subtree(const Shape &S, int l) {
+    if (l >= S.L) return 0;
+    if (S.kind == kShapeBalanced) return S.N >> l;  // the upper child of n points has floor(n/2)
+    return seg_size(S, l, full_nodes(l));           // the first subtree of a level is the largest
+}
+
+// 32-bit forms of ss and sb for device code (left-balanced shape): with
+// N < 2^31 every node id, size and position fits; requires l < L and s on
+// level l.
 __device__ __forceinline__ int32_t seg_size32(const Shape &S, int l, int32_t s) {
     if (s >= (int32_t)S.N) return 0;
     const int32_t B = 1 << (S.L - 1 - l);
@@ -92,9 +150,11 @@ __device__ __forceinline__ int32_t seg_begin32(const Shape &S, int l, int32_t s)
     return ((1 << l) - 1) + j * (B - 1) + (t < (int32_t)S.M ? t : (int32_t)S.M);
 }
 
-// Number of nodes that exist on level l.
+// Number of node slots of level l that the build visits (left-balanced: the
+// nodes that exist; balanced: every slot of the level).
 __host__ __device__ __forceinline__ int64_t nodes_on_level(const Shape &S, int l) {
     const int64_t w = (int64_t)1 << l;
+    if (S.kind == kShapeBalanced) return w;
     const int64_t left = S.N - full_nodes(l);
     return left < w ? left : w;
 }
@@ -198,7 +258,9 @@ struct Plan {
     size_t bytes;
 };
 
-int make_plan(int64_t N, int k, int mode, Plan *p);
+// shape: kShapeLeftBalanced (either split rule) or kShapeBalanced (the
+// round-robin rule only).
+int make_plan(int64_t N, int k, int mode, Plan *p, int shape = kShapeLeftBalanced);
 
 struct Buffers {
     int *status;

@@ -86,6 +86,15 @@ __device__ uint32_t first_key_at_least(const Bucketer &bk, uint32_t b) {
 
 // Subtree of level l that holds array position p (inverse of sb).
 __device__ __forceinline__ int64_t seg_of_pos(const Shape &S, int l, int64_t p) {
+    if (S.kind == kShapeBalanced) {  // sb increases along the level: binary search, O(l^2)
+        int64_t lo = 0, hi = ((int64_t)1 << l) - 1;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (seg_begin(S, l, full_nodes(l) + mid) <= p) lo = mid;
+            else hi = mid - 1;
+        }
+        return full_nodes(l) + lo;
+    }
     const int64_t B = (int64_t)1 << (S.L - 1 - l), A = B - 1;
     const int64_t q = p - full_nodes(l);
     const int64_t nf = S.M / B;          // subtrees with a full last-level part

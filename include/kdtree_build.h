@@ -135,6 +135,39 @@ int kdt_build_inplace(float *pts, int64_t N, int k, int split_mode,
                       int32_t *perm, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* ---- the balanced tree of Brown's builder ---------------------------------
+ * "An Implementation of a Balanced Kd Tree Builder Using GPUs", overview
+ * list: sort one reference array per coordinate, take the median of the
+ * first coordinate's array as the first node, partition the other arrays into
+ * the points below and above it, and repeat on both sides with the next
+ * coordinate, cycling through the coordinates; build section: the medians of
+ * level L form a per-level store whose entry j has its children at entries 2j
+ * and 2j+1 of level L+1.  This tree is balanced but not left-balanced: a node
+ * of n points keeps the point of rank floor((n-1)/2) under the split order
+ * (dimension level mod k; the same strict super key + input index order as
+ * above, so duplicates are kept and the tree is unique), its lower subtree
+ * gets floor((n-1)/2) points and its upper subtree the rest.
+ *
+ * Storage: heap order, the node of entry j of level L in slot 2^L - 1 + j;
+ * slots[s] = input index of the point at slot s, -1 where the subtree is
+ * empty.  The tree has numLevels(N) levels, so slots has
+ * kdt_balanced_slots(N) = 2^numLevels(N) - 1 entries (< 2N). */
+
+/* Number of heap slots of the balanced tree of N points.  Host-only. */
+int kdt_balanced_slots(int64_t N, int64_t *slots);
+
+/* Bytes of device scratch for kdt_build_balanced.  Host-only. */
+int kdt_balanced_workspace_size(int64_t N, int k, size_t *bytes);
+
+/* Builds the balanced tree.  pts (N x k float32, read-only), slots
+ * (int32[kdt_balanced_slots(N)], fully overwritten) and workspace (at least
+ * kdt_balanced_workspace_size bytes, 256-byte aligned, not in use by another
+ * call until this one completes on `stream`) are DEVICE pointers owned by the
+ * caller.  Same limits and errors as kdt_build.  Allocates nothing.
+ * Stream-ordered. */
+int kdt_build_balanced(const float *pts, int64_t N, int k, int32_t *slots,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---- queries on a built tree ------------------------------------------------
  * tree_pts is the tree's points in level order (row u = the point stored at
  * node u: the output of kdt_gather_points or kdt_build_inplace), N x k float32,

@@ -87,3 +87,18 @@ def test_kernel_stat_struct_matches_the_header(lib):
     want = [(name, ctype_of[t.strip()]) for t, name in fields]
     assert kdt._KernelStat._fields_ == want
     assert ctypes.sizeof(kdt._KernelStat) == 40
+
+
+def test_balanced_entry_points_argument_checks(lib):
+    out = ctypes.c_int64(0)
+    for n, want in [(1, 1), (2, 3), (3, 3), (4, 7), (1000, 1023), (2**31 - 1, 2**31 - 1)]:
+        assert lib.kdt_balanced_slots(n, ctypes.byref(out)) == kdt.OK
+        assert out.value == want
+    assert lib.kdt_balanced_slots(0, ctypes.byref(out)) == kdt.EINVAL
+    assert lib.kdt_balanced_slots(10, None) == kdt.EINVAL
+    sz = ctypes.c_size_t(0)
+    assert lib.kdt_balanced_workspace_size(10, 3, ctypes.byref(sz)) == kdt.OK and sz.value > 0
+    assert lib.kdt_balanced_workspace_size(10, kdt_max_k() + 1, ctypes.byref(sz)) == kdt.EINVAL
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.kdt_build_balanced(None, 10, 3, fake, fake, 1 << 20, None) == kdt.EINVAL
+    assert lib.kdt_build_balanced(fake, 10, 3, fake, ctypes.c_void_p(0x100000), 1, None) == kdt.ENOMEM
