@@ -189,6 +189,17 @@ int kdt_host_workspace_size(int64_t N, int k, int split_mode, size_t *bytes) {
     return KDT_OK;
 }
 
+// Device-side address of a page-locked host buffer, or nullptr if the buffer
+// is ordinary pageable memory (or the device cannot address it).
+static const void *pinned_device_address(const void *host) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode, int32_t *host_perm, void *workspace,
                    size_t workspace_bytes, void *stream) {
     if (!host_pts || !host_perm || !workspace) return KDT_EINVAL;
@@ -204,11 +215,21 @@ int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode, int3
     float *d_pts = reinterpret_cast<float *>(base + p.bytes);
     int32_t *d_perm = reinterpret_cast<int32_t *>(base + p.bytes + ((size_t)N * k * 4 + 255) / 256 * 256);
     const Buffers b = carve(p, workspace);
-    if (cudaMemcpyAsync(d_pts, host_pts, (size_t)N * k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return KDT_ECUDA;
-    rc = enqueue_build(p, b, d_pts, d_perm, s);
+    // Page-locked host buffers are used in place: the first kernel reads the
+    // points across the host link as it converts them, and the kernels that
+    // fix nodes write the permutation straight into host memory, so the
+    // transfers overlap the build instead of preceding and following it.
+    // Pageable buffers are staged through the workspace.
+    const float *pts_in = static_cast<const float *>(pinned_device_address(host_pts));
+    int32_t *perm_out = static_cast<int32_t *>(const_cast<void *>(pinned_device_address(host_perm)));
+    if (!pts_in) {
+        if (cudaMemcpyAsync(d_pts, host_pts, (size_t)N * k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return KDT_ECUDA;
+        pts_in = d_pts;
+    }
+    rc = enqueue_build(p, b, pts_in, perm_out ? perm_out : d_perm, s);
     if (rc != KDT_OK) return rc;
-    if (cudaMemcpyAsync(host_perm, d_perm, (size_t)N * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (!perm_out && cudaMemcpyAsync(host_perm, d_perm, (size_t)N * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return KDT_ECUDA;
     int st = 0;
     if (cudaMemcpyAsync(&st, b.status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KDT_ECUDA;

@@ -128,6 +128,7 @@ struct LevelArgs {
     uint32_t *hist_nxt;  // children's histograms (fused next level) or null
     SegSel *sel;
     int hist_in;         // per-subtree levels: this level's histograms were built by the level above
+    int warp_res;        // partition: each warp reserves its own output ranges (no CTA barriers)
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
     int64_t ld;          // records per group column
@@ -263,22 +264,34 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         tL += __popc(mV[i] & ~mR[i]);
         tR += __popc(mR[i]);
     }
-    if (lane == 0) {
-        wtot[2 * w + 0] = tL;
-        wtot[2 * w + 1] = tR;
-    }
-    __syncthreads();
-    if (tid < 2u) {  // side tid: one cursor reservation, then the warps' offsets
-        uint32_t sum = 0u;
-        for (uint32_t v = 0; v < nw; ++v) sum += wtot[2 * v + tid];
-        uint32_t base = sum ? atomicAdd(&cursors[tid ? 2 : 0], sum) : 0u;
-        for (uint32_t v = 0; v < nw; ++v) {
-            wbase[2 * v + tid] = base;
-            base += wtot[2 * v + tid];
+    uint32_t oL, oR;
+    if (a.warp_res) {  // one reservation per warp and side (cursors spread over many subtrees, or in shared memory)
+        uint32_t bL = 0u, bR = 0u;
+        if (lane == 0) {
+            if (tL) bL = atomicAdd(&cursors[0], tL);
+            if (tR) bR = atomicAdd(&cursors[2], tR);
         }
+        oL = __shfl_sync(0xffffffffu, bL, 0);
+        oR = __shfl_sync(0xffffffffu, bR, 0);
+    } else {  // one reservation per CTA and side, then the warps' offsets
+        if (lane == 0) {
+            wtot[2 * w + 0] = tL;
+            wtot[2 * w + 1] = tR;
+        }
+        __syncthreads();
+        if (tid < 2u) {
+            uint32_t sum = 0u;
+            for (uint32_t v = 0; v < nw; ++v) sum += wtot[2 * v + tid];
+            uint32_t base = sum ? atomicAdd(&cursors[tid ? 2 : 0], sum) : 0u;
+            for (uint32_t v = 0; v < nw; ++v) {
+                wbase[2 * v + tid] = base;
+                base += wtot[2 * v + tid];
+            }
+        }
+        __syncthreads();
+        oL = wbase[2 * w + 0];
+        oR = wbase[2 * w + 1];
     }
-    __syncthreads();
-    uint32_t oL = wbase[2 * w + 0], oR = wbase[2 * w + 1];
     const uint32_t lbeg = (uint32_t)g.left_begin, rtail = (uint32_t)pp.right_tail;
     const uint32_t cgap = lbeg + pp.below, s32 = (uint32_t)g.s;
     // pos: destination position of each point (32 bit); side 3 = not stored
@@ -730,6 +743,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.hist_cur = b.hist[l & 1];
     a.hist_nxt = nullptr;
     a.hist_in = 0;
+    a.warp_res = 0;  // multi-CTA levels: one global reservation per CTA and tile
     a.sel = b.sel;
     a.status = b.status;
     a.per_cta = 0;
@@ -772,6 +786,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     } else {
         // the level above built this level's histograms if it could
         a.hist_in = fusable && l > 0 ? 1 : 0;
+        a.warp_res = 1;  // cursors in shared memory
         if (l + 1 < p.finish_level && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
         ProfScope ps(stream, "seg", alg);
         level_seg_kernel<<<(unsigned)nseg, kPartThreads, 0, stream>>>(a);

@@ -393,6 +393,32 @@ def workload_rows(kdt, dev, stream, peak, names, steps: int, oracle_full: bool) 
     return rows
 
 
+def balanced_extra(kdt, pts, workload, stream, steps: int = 5) -> dict:
+    """Times kdt_build_balanced (the median-split tree of Brown's builder,
+    round-robin split) on the bench workload's points, device-resident, with
+    a caller workspace; CUDA events over `steps` builds after 2 warm-ups."""
+    import torch
+    n, k = pts.shape
+    out = torch.empty(kdt.balanced_slots(n), dtype=torch.int32, device=pts.device)
+    ws = torch.empty(kdt.balanced_workspace_bytes(n, k), dtype=torch.uint8, device=pts.device)
+
+    def step():
+        kdt.build_balanced(pts, out=out, workspace=ws, stream=stream)
+
+    for _ in range(2):
+        step()
+    ms = time_steps(step, stream, steps) / steps
+    if kdt.status(stream) != 0:
+        raise SystemExit("device status after the balanced builds")
+    nodes = int((out >= 0).sum().item())
+    if nodes != n:
+        raise SystemExit("balanced tree: occupied slots != N")
+    balg = b_alg(n)
+    return {"ms": ms, "points_per_s": n / (ms / 1e3), "slots": out.numel(), "split_rule": "round_robin",
+            "frac_of_measured_B_alg": balg / (ms / 1e3) / 1e9 / measured_peaks()[0],
+            "api": "kdt_build_balanced (lower median, heap-ordered slots)"}
+
+
 def run_ours(args, workload):
     import torch
     import balanced_tree_build_gb300 as kdt
@@ -504,6 +530,8 @@ def run_ours(args, workload):
         lo, tree_pts = level_order_extra(kdt, pts, perm, ws, workload, stream, peak)
         extras = {"level_order_points": lo, "knn": knn_extra(kdt, tree_pts, workload, stream)}
         del tree_pts
+        if workload.mode == 0:
+            extras["balanced_tree"] = balanced_extra(kdt, pts, workload, stream)
     if not args.no_workloads and rank == 0:
         del ws
         torch.cuda.empty_cache()

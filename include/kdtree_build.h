@@ -91,11 +91,13 @@ int kdt_build_ws(const float *pts, int64_t N, int k, int split_mode,
                  int32_t *perm, void *workspace, size_t workspace_bytes,
                  void *stream);
 
-/* Host-buffer variant: host_pts and host_perm are HOST pointers (pinned memory
- * gives asynchronous copies; pageable memory works but is staged by CUDA).
- * Device scratch is `workspace` (at least kdt_host_workspace_size() bytes),
- * which also receives the copied points and the device-side permutation.
- * Copies the points to the device, builds, copies the permutation back.
+/* Host-buffer variant: host_pts and host_perm are HOST pointers.  Page-locked
+ * (pinned) buffers are used in place: the build's first kernel reads the
+ * points across the host link while converting them, and the kernels that fix
+ * nodes write the permutation straight into host_perm, so the transfers
+ * overlap the build.  Pageable buffers are staged: the points are copied into
+ * `workspace` first and the permutation is copied back at the end.  Device
+ * scratch is `workspace` (at least kdt_host_workspace_size() bytes).
  * Synchronous; returns device-side errors directly. */
 int kdt_host_workspace_size(int64_t N, int k, int split_mode, size_t *bytes);
 int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode,
