@@ -131,6 +131,85 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
     }
 }
 
+// k = 3, points 16-byte aligned: four points are three 128-bit loads, and two
+// such groups per thread are in flight at once.  Besides the records, the
+// first coordinate's keys go to a dense column (`col0`, may be null) that the
+// first level's histogram reads instead of the 16-byte records.
+constexpr int kInit3Threads = 256;
+
+__device__ __forceinline__ void init3_point(float x, float y, float z, uint32_t i, uint4 &r, uint32_t *mn,
+                                            uint32_t *mx, int &bad) {
+    bad |= !isfinite(x) | !isfinite(y) | !isfinite(z);
+    r.x = f2key(x);
+    r.y = f2key(y);
+    r.z = f2key(z);
+    r.w = i;
+    mn[0] = min(mn[0], r.x);
+    mx[0] = max(mx[0], r.x);
+    mn[1] = min(mn[1], r.y);
+    mx[1] = max(mx[1], r.y);
+    mn[2] = min(mn[2], r.z);
+    mx[2] = max(mx[2], r.z);
+}
+
+__global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__restrict__ pts, int64_t N,
+                                                                 uint4 *__restrict__ rec, uint32_t *__restrict__ col0,
+                                                                 uint32_t *__restrict__ bbox,
+                                                                 int *__restrict__ status) {
+    uint32_t mn[3] = {0xffffffffu, 0xffffffffu, 0xffffffffu}, mx[3] = {0u, 0u, 0u};
+    int bad = 0;
+    const int64_t groups = N >> 2;  // groups of four points
+    const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+    const uint4 *p4 = reinterpret_cast<const uint4 *>(pts);
+    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += 2 * nt) {
+        uint4 v[2][3];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t g = g0 + u * nt;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) v[u][j] = g < groups ? __ldg(p4 + 3 * g + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t g = g0 + u * nt;
+            if (g >= groups) continue;
+            float f[12];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                f[4 * j + 0] = __uint_as_float(v[u][j].x);
+                f[4 * j + 1] = __uint_as_float(v[u][j].y);
+                f[4 * j + 2] = __uint_as_float(v[u][j].z);
+                f[4 * j + 3] = __uint_as_float(v[u][j].w);
+            }
+            uint4 r[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                init3_point(f[3 * i], f[3 * i + 1], f[3 * i + 2], (uint32_t)(4 * g + i), r[i], mn, mx, bad);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rec[4 * g + i] = r[i];
+            if (col0) reinterpret_cast<uint4 *>(col0)[g] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
+        }
+    }
+    // the last N mod 4 points
+    const int64_t tail = (int64_t)blockIdx.x * blockDim.x + threadIdx.x + (groups << 2);
+    if (tail < N) {
+        uint4 r;
+        init3_point(pts[3 * tail], pts[3 * tail + 1], pts[3 * tail + 2], (uint32_t)tail, r, mn, mx, bad);
+        rec[tail] = r;
+        if (col0) col0[tail] = r.x;
+    }
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
+        const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(&bbox[c], a);
+            atomicMax(&bbox[3 + c], b);
+        }
+    }
+}
+
 // Root node table entry: domain = bounding box of all points, dim = widest.
 __global__ void root_table_kernel(const uint32_t *bbox, int k, float *dom, int *dim) {
     float lo[kMaxK], hi[kMaxK];
@@ -186,7 +265,8 @@ int make_plan(int64_t N, int k, int mode, Plan *p, int shape) {
         q.off_dim[b] = off;
         off = align_up(off + (size_t)q.table_cap * 4, 256);
         q.off_hist[b] = off;
-        off = align_up(off + (size_t)q.hist_rows * kBuckets * 4, 256);
+        const int64_t words = q.hist_rows * kBuckets;
+        off = align_up(off + (size_t)(b == 0 && words < kBuckets0 ? kBuckets0 : words) * 4, 256);  // level 0: kBuckets0
     }
     q.off_sel = off;
     off = align_up(off + (size_t)q.sel_cap * sizeof(SegSel), 256);
@@ -203,6 +283,7 @@ Buffers carve(const Plan &p, void *base) {
     r.status = reinterpret_cast<int *>(b + p.off_status);
     r.bbox = reinterpret_cast<uint32_t *>(b + p.off_bbox);
     for (int i = 0; i < 3; ++i) r.rec[i] = reinterpret_cast<uint4 *>(b + p.off_rec[i]);
+    r.col0 = nullptr;
     for (int i = 0; i < 2; ++i) {
         r.dom[i] = reinterpret_cast<float *>(b + p.off_dom[i]);
         r.dim[i] = reinterpret_cast<int *>(b + p.off_dim[i]);
@@ -219,7 +300,8 @@ Buffers carve(const Plan &p, void *base) {
         if (e_ != cudaSuccess) return KDT_ECUDA;                \
     } while (0)
 
-int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *perm, cudaStream_t stream) {
+int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t *perm, cudaStream_t stream) {
+    Buffers b = b_in;
     const Shape &S = p.S;
     const int k = p.k;
     const double Nd = (double)S.N;
@@ -238,7 +320,18 @@ int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *pe
         const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 16;
         if (blocks > cap) blocks = cap;
         ProfScope ps(stream, "init", 0.0);
-        if (k <= 3)
+        if (k == 3 && (reinterpret_cast<uintptr_t>(pts) & 15u) == 0) {
+            // the first level's histogram reads a dense copy of the first
+            // coordinate's keys, kept in the candidate buffer until that level
+            uint32_t *col0 = p.finish_level > 0 && p.mode == KDT_SPLIT_ROUND_ROBIN
+                                 ? reinterpret_cast<uint32_t *>(b.rec[2]) : nullptr;
+            b.col0 = col0;
+            int64_t g3 = (S.N / 4 + 2 * kInit3Threads - 1) / (2 * kInit3Threads);
+            const int64_t cap3 = (int64_t)(sms > 0 ? sms : 152) * 16;
+            if (g3 > cap3) g3 = cap3;
+            if (g3 < 1) g3 = 1;
+            init3_kernel<<<(unsigned)g3, kInit3Threads, 0, stream>>>(pts, S.N, b.rec[0], col0, b.bbox, b.status);
+        } else if (k <= 3)
             init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);
         else if (k <= 8)

@@ -240,6 +240,7 @@ struct SegSel {
 };
 
 constexpr int kBuckets = 2048;         // value buckets per subtree on global levels
+constexpr int kBuckets0 = 16384;       // value buckets of level 0 (one subtree, its own histogram pass)
 constexpr int kMultiMaxSegs = 1024;    // multi-CTA levels: at most this many subtrees
 
 struct Plan {
@@ -266,6 +267,7 @@ struct Buffers {
     int *status;
     uint32_t *bbox;  // [2k]: min keys then max keys
     uint4 *rec[3];   // record buffers: [0], [1] ping-pong, [2] bucket candidates
+    const uint32_t *col0;  // dense keys of coordinate 0 for the first level's histogram, or null
     float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
     int *dim[2];
     uint32_t *hist[2];  // [rows][kBuckets]

@@ -41,6 +41,7 @@ constexpr int kTile = kPartThreads * kEPT;
 
 struct Bucketer {
     float lo, scale;
+    int nb;  // number of buckets
     // Monotone non-decreasing in the coordinate: fsub and fmul round to
     // nearest (monotone), truncation and clamping are monotone.
     __device__ __forceinline__ int operator()(uint32_t key) const {
@@ -48,20 +49,21 @@ struct Bucketer {
         const float t = __fmul_rn(__fsub_rn(x, lo), scale);
         int b = __float2int_rz(t);
         b = b < 0 ? 0 : b;
-        return b < kBuckets ? b : kBuckets - 1;
+        return b < nb ? b : nb - 1;
     }
 };
 
-__device__ __forceinline__ Bucketer make_bucketer(float lo, float hi) {
+__device__ __forceinline__ Bucketer make_bucketer(float lo, float hi, int nb = kBuckets) {
     const float r = __fsub_rn(hi, lo);
     float scale = 0.f;  // empty or non-finite range: every point in bucket 0
     if (r > 0.f && r <= 3.0e38f) {
-        scale = __fdiv_rn((float)kBuckets, r);
+        scale = __fdiv_rn((float)nb, r);
         if (!(scale <= 3.0e38f)) scale = 0.f;
     }
     Bucketer b;
     b.lo = lo;
     b.scale = scale;
+    b.nb = nb;
     return b;
 }
 
@@ -74,7 +76,7 @@ constexpr uint32_t kKeyMin = 0x00800000u, kKeyMax = 0xff7fffffu;
 // points of buckets < b are exactly the keys below it (binary search on the
 // monotone bucket function).
 __device__ uint32_t first_key_at_least(const Bucketer &bk, uint32_t b) {
-    if (b >= (uint32_t)kBuckets) return kKeyMax + 1u;
+    if (b >= (uint32_t)bk.nb) return kKeyMax + 1u;
     uint32_t lo = kKeyMin, hi = kKeyMax + 1u;
     while (lo < hi) {
         const uint32_t mid = lo + (hi - lo) / 2u;
@@ -124,11 +126,13 @@ struct LevelArgs {
     const int *dim_cur;
     float *dom_nxt;
     int *dim_nxt;
-    uint32_t *hist_cur;  // [subtrees][kBuckets] (multi-CTA levels)
+    uint32_t *hist_cur;  // [subtrees][nbk] (multi-CTA levels)
+    int nbk;             // buckets of this level's histogram (kBuckets0 on level 0, else kBuckets)
     uint32_t *hist_nxt;  // children's histograms (fused next level) or null
     SegSel *sel;
     int hist_in;         // per-subtree levels: this level's histograms were built by the level above
     int warp_res;        // partition: each warp reserves its own output ranges (no CTA barriers)
+    const uint32_t *col0;  // level 0, round-robin: dense keys of the split coordinate (else null)
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
     int64_t ld;          // records per group column
@@ -153,9 +157,9 @@ __device__ __forceinline__ SegInfo seg_info(const LevelArgs &a, int64_t s) {
     return g;
 }
 
-__device__ __forceinline__ Bucketer seg_bucketer(const LevelArgs &a, int64_t j, int d) {
+__device__ __forceinline__ Bucketer seg_bucketer(const LevelArgs &a, int64_t j, int d, int nb = kBuckets) {
     const float *dom = a.dom_cur + j * 2 * a.k;
-    return make_bucketer(dom[d], dom[a.k + d]);
+    return make_bucketer(dom[d], dom[a.k + d], nb);
 }
 
 __device__ __forceinline__ bool stop_requested(const int *status, int *flag) {
@@ -476,11 +480,13 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
     }
 }
 
-// Picks the bucket holding rank m from a histogram of kBuckets counts
-// (CTA-wide).  Returns false if the counts do not add up to n.
-__device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out) {
+// Picks the bucket holding rank m from a histogram of nb counts (CTA-wide;
+// nb a multiple of the CTA size).  Returns false if the counts do not add up
+// to n.
+__device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out,
+                            int nb = kBuckets) {
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
-    const uint32_t per = kBuckets / nt;
+    const uint32_t per = (uint32_t)nb / nt;
     uint32_t sum = 0;
     for (uint32_t i = 0; i < per; ++i) sum += H[tid * per + i];
     uint32_t total;
@@ -507,7 +513,7 @@ __device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t 
 // `hist`; each thread issues eight loads before its atomics (the records are
 // in global memory; col points at word d of record 0, stride 4 words).
 __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64_t e, const Bucketer &bk,
-                                           uint32_t *hist) {
+                                           uint32_t *hist, int stride = 4) {
     constexpr int kH = 8;
     const uint32_t nt = blockDim.x;
     for (int64_t q0 = b + threadIdx.x; q0 < e; q0 += (int64_t)kH * nt) {
@@ -515,7 +521,7 @@ __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64
 #pragma unroll
         for (int u = 0; u < kH; ++u) {
             const int64_t q = q0 + (int64_t)u * nt;
-            v[u] = q < e ? __ldg(col + 4 * q) : 0u;
+            v[u] = q < e ? __ldg(col + stride * q) : 0u;
         }
 #pragma unroll
         for (int u = 0; u < kH; ++u)
@@ -526,7 +532,7 @@ __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64
 // ---- multi-CTA pipeline kernels ----------------------------------------------
 
 __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
-    __shared__ uint32_t hist[kBuckets];
+    extern __shared__ uint32_t hist[];  // [a.nbk]
     __shared__ int stop;
     if (stop_requested(a.status, &stop)) return;
     const int64_t begin = full_nodes(a.l) + (int64_t)blockIdx.x * a.per_cta;
@@ -536,14 +542,18 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
         const int64_t s = seg_of_pos(a.S, a.l, p);
         const SegInfo g = seg_info(a, s);
         const int64_t pe = min(end, g.base + (int64_t)g.n);
-        const Bucketer bk = seg_bucketer(a, g.j, g.d);
-        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x) hist[b] = 0u;
+        const Bucketer bk = seg_bucketer(a, g.j, g.d, a.nbk);
+        for (uint32_t b = threadIdx.x; b < (uint32_t)a.nbk; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
-        hist_range(col, p, pe, bk, hist);
+        if (a.col0 != nullptr) {  // level 0: the dense column of the split coordinate
+            hist_range(a.col0, p, pe, bk, hist, 1);
+        } else {
+            const uint32_t *col = reinterpret_cast<const uint32_t *>(a.src + (int64_t)(g.d >> 2) * ld) + (g.d & 3);
+            hist_range(col, p, pe, bk, hist);
+        }
         __syncthreads();
-        uint32_t *H = a.hist_cur + g.j * kBuckets;
-        for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += blockDim.x)
+        uint32_t *H = a.hist_cur + g.j * a.nbk;
+        for (uint32_t b = threadIdx.x; b < (uint32_t)a.nbk; b += blockDim.x)
             if (hist[b]) atomicAdd(&H[b], hist[b]);
         __syncthreads();
         p = pe;
@@ -557,10 +567,10 @@ __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
     if (stop_requested(a.status, &stop)) return;
     const int64_t s = full_nodes(a.l) + blockIdx.x;
     const SegInfo g = seg_info(a, s);
-    const bool ok = pick_bucket(a.hist_cur + g.j * kBuckets, g.n, g.m, red, &pp);
+    const bool ok = pick_bucket(a.hist_cur + g.j * a.nbk, g.n, g.m, red, &pp, a.nbk);
     // key bounds of the split bucket: two binary searches in two warps
-    if (threadIdx.x == 32) pp.khi = first_key_at_least(seg_bucketer(a, g.j, g.d), pp.bstar + 1u);
-    if (threadIdx.x == 0) pp.klo = first_key_at_least(seg_bucketer(a, g.j, g.d), pp.bstar);
+    if (threadIdx.x == 32) pp.khi = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar + 1u);
+    if (threadIdx.x == 0) pp.klo = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar);
     __syncthreads();
     if (threadIdx.x == 0) {
         if (!ok) set_status(a.status, KDT_EINTERNAL);
@@ -742,8 +752,10 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.dim_nxt = b.dim[(l + 1) & 1];
     a.hist_cur = b.hist[l & 1];
     a.hist_nxt = nullptr;
+    a.nbk = kBuckets;
     a.hist_in = 0;
     a.warp_res = 0;  // multi-CTA levels: one global reservation per CTA and tile
+    a.col0 = l == 0 ? b.col0 : nullptr;
     a.sel = b.sel;
     a.status = b.status;
     a.per_cta = 0;
@@ -763,9 +775,16 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         const bool fused_here = l > 0 && fusable;
         if (l + 1 < p.finish_level && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
         if (!fused_here) {
-            if (cudaMemsetAsync(a.hist_cur, 0, (size_t)nseg * kBuckets * 4, stream) != cudaSuccess) return KDT_ECUDA;
+            // level 0 (one subtree) takes a finer histogram: fewer candidates
+            // for the one CTA that resolves its split
+            a.nbk = l == 0 ? kBuckets0 : kBuckets;
+            if (cudaMemsetAsync(a.hist_cur, 0, (size_t)nseg * a.nbk * 4, stream) != cudaSuccess) return KDT_ECUDA;
+            const size_t hsm = (size_t)a.nbk * 4;
+            if (cudaFuncSetAttribute(level_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm) !=
+                cudaSuccess)
+                return KDT_ECUDA;
             ProfScope ps(stream, "hist", 0.0);
-            level_hist_kernel<<<(unsigned)nblk, kLvlThreads, 0, stream>>>(a);
+            level_hist_kernel<<<(unsigned)nblk, kLvlThreads, hsm, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         {
