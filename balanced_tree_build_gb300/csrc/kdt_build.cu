@@ -268,8 +268,10 @@ int make_plan(int64_t N, int k, int mode, Plan *p, int shape) {
         const int64_t words = q.hist_rows * kBuckets;
         off = align_up(off + (size_t)(b == 0 && words < kBuckets0 ? kBuckets0 : words) * 4, 256);  // level 0: kBuckets0
     }
-    q.off_sel = off;
-    off = align_up(off + (size_t)q.sel_cap * sizeof(SegSel), 256);
+    for (int t = 0; t < 2; ++t) {
+        q.off_sel[t] = off;
+        off = align_up(off + (size_t)q.sel_cap * sizeof(SegSel), 256);
+    }
     q.off_fb = off;
     off = align_up(off + (size_t)q.table_cap, 256);
     q.bytes = off;
@@ -289,7 +291,8 @@ Buffers carve(const Plan &p, void *base) {
         r.dim[i] = reinterpret_cast<int *>(b + p.off_dim[i]);
         r.hist[i] = reinterpret_cast<uint32_t *>(b + p.off_hist[i]);
     }
-    r.sel = reinterpret_cast<SegSel *>(b + p.off_sel);
+    r.sel[0] = reinterpret_cast<SegSel *>(b + p.off_sel[0]);
+    r.sel[1] = reinterpret_cast<SegSel *>(b + p.off_sel[1]);
     r.fallback = b + p.off_fb;
     return r;
 }

@@ -252,10 +252,10 @@ struct Plan {
     TilePlan tp;
     int64_t table_cap;   // node-table entries per level
     int64_t hist_rows;   // histogram rows per buffer (multi-CTA levels)
-    int64_t sel_cap;     // SegSel entries
+    int64_t sel_cap;     // SegSel entries per table (two tables, by level parity)
     int64_t ld;          // records per group column (N rounded up to 8)
     // byte offsets inside the workspace
-    size_t off_status, off_bbox, off_rec[3], off_dom[2], off_dim[2], off_hist[2], off_sel, off_fb;
+    size_t off_status, off_bbox, off_rec[3], off_dom[2], off_dim[2], off_hist[2], off_sel[2], off_fb;
     size_t bytes;
 };
 
@@ -271,7 +271,7 @@ struct Buffers {
     float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
     int *dim[2];
     uint32_t *hist[2];  // [rows][kBuckets]
-    SegSel *sel;
+    SegSel *sel[2];     // per live subtree of a global level, by level parity
     uint8_t *fallback;  // [tiles]: 1 = tile left to the select finisher
 };
 

@@ -33,7 +33,9 @@ namespace kdt {
 
 constexpr int kLvlThreads = 512;
 constexpr int kPickThreads = 256;
-constexpr int kEPT = 4;                          // consecutive points per thread per tile
+constexpr int kEPT = 4;                          // consecutive points per thread per tile (divides 8: rows up to
+                                                 // the next multiple of 8 exist in every record buffer)
+constexpr int kPartCtas = 8;                     // partition CTAs per SM
 constexpr int kPartThreads = 128;                // partition CTAs (multi-CTA and per-subtree)
 constexpr int kTile = kPartThreads * kEPT;
 
@@ -133,6 +135,11 @@ struct LevelArgs {
     int hist_in;         // per-subtree levels: this level's histograms were built by the level above
     int warp_res;        // partition: each warp reserves its own output ranges (no CTA barriers)
     const uint32_t *col0;  // level 0, round-robin: dense keys of the split coordinate (else null)
+    // resolve: pick the next level's split buckets for this subtree's two
+    // children (their histograms are final once its candidates are added)
+    int pick_next;
+    SegSel *sel_next;      // the next level's selections
+    uint32_t *hist_nn;     // histograms of the level after next (cleared for the grandchildren), or null
     int *status;
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
     int64_t ld;          // records per group column
@@ -240,9 +247,9 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const uint32_t lane = tid & 31u, w = tid >> 5, nw = nt >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    const uint32_t q0 = (uint32_t)t0 + 4u * tid;
+    const uint32_t q0 = (uint32_t)t0 + (uint32_t)kEPT * tid;
     const uint32_t vb32 = (uint32_t)vb, ve32 = (uint32_t)ve;
-    const bool any = q0 + 4u > vb32 && q0 < ve32;
+    const bool any = q0 + (uint32_t)kEPT > vb32 && q0 < ve32;
     // group 0 of the thread's four records (for k <= 3 the whole record);
     // rows up to q0 + 3 < ld exist in every buffer
     uint4 r[kEPT];
@@ -560,12 +567,11 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
-    __shared__ uint32_t red[64];
-    __shared__ PartPlan pp;
-    __shared__ int stop;
-    if (stop_requested(a.status, &stop)) return;
-    const int64_t s = full_nodes(a.l) + blockIdx.x;
+// CTA-wide: the split bucket of subtree s of level a.l from its histogram
+// (a.nbk buckets), written to a.sel[j] with cleared cursors; with a.hist_nxt
+// set, the children's histogram rows of the next level are cleared too.
+// `pp` and `red` are shared scratch.
+__device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32_t *red) {
     const SegInfo g = seg_info(a, s);
     const bool ok = pick_bucket(a.hist_cur + g.j * a.nbk, g.n, g.m, red, &pp, a.nbk);
     // key bounds of the split bucket: two binary searches in two warps
@@ -587,6 +593,15 @@ __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
         uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
         for (uint32_t t = threadIdx.x; t < 2u * kBuckets; t += blockDim.x) H[t] = 0u;
     }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
+    __shared__ uint32_t red[64];
+    __shared__ PartPlan pp;
+    __shared__ int stop;
+    if (stop_requested(a.status, &stop)) return;
+    pick_subtree(a, full_nodes(a.l) + blockIdx.x, pp, red);
 }
 
 __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, uint32_t below, uint32_t cnt,
@@ -602,7 +617,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
     return pp;
 }
 
-__global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(LevelArgs a) {
     __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
@@ -626,7 +641,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_part_kernel(LevelArgs a
             for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) fh[b] = 0u;
         }
         __syncthreads();
-        for (int64_t t0 = p & ~(int64_t)3; t0 < pe; t0 += kTile) {
+        for (int64_t t0 = p & ~(int64_t)(kEPT - 1); t0 < pe; t0 += kTile) {
             if (t0 + 2 * kTile < pe) prefetch_tile(a, t0 + 2 * kTile, pe);
             part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         }
@@ -658,6 +673,23 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
         return;
     }
     resolve_segment(a, g, pp, st, hist, red, medw, cur2, a.hist_nxt != nullptr, (a.l + 1) % a.k);
+    if (a.pick_next && !st.err) {
+        // the children's histograms are final now (the part pass flushed its
+        // counts before this kernel; this CTA added the candidates'), and so
+        // are their domains: pick the next level's split buckets here
+        __shared__ PartPlan ppn;
+        __syncthreads();
+        LevelArgs an = a;
+        an.l = a.l + 1;
+        an.dom_cur = a.dom_nxt;
+        an.dim_cur = a.dim_nxt;
+        an.hist_cur = a.hist_nxt;
+        an.hist_nxt = a.hist_nn;
+        an.sel = a.sel_next;
+        an.nbk = kBuckets;
+        pick_subtree(an, 2 * s + 1, ppn, red);
+        pick_subtree(an, 2 * s + 2, ppn, red);
+    }
 }
 
 // ---- one CTA per subtree -------------------------------------------------------
@@ -713,7 +745,7 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
     bkc.lo = 0.f;
     bkc.scale = 0.f;
     if (fuse) bkc = seg_bucketer(a, g.j, dn);  // the children's: the parent's domain in dn
-    for (int64_t t0 = g.base & ~(int64_t)3; t0 < g.base + (int64_t)g.n; t0 += kTile) {
+    for (int64_t t0 = g.base & ~(int64_t)(kEPT - 1); t0 < g.base + (int64_t)g.n; t0 += kTile) {
         if (t0 + 2 * kTile < g.base + (int64_t)g.n) prefetch_tile(a, t0 + 2 * kTile, g.base + (int64_t)g.n);
         part_tile(a, g, bk, pp, t0, g.base, g.base + (int64_t)g.n, cursors, wtot, wbase, fuse ? fh : nullptr, bkc,
                   dn);
@@ -756,7 +788,10 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.hist_in = 0;
     a.warp_res = 0;  // multi-CTA levels: one global reservation per CTA and tile
     a.col0 = l == 0 ? b.col0 : nullptr;
-    a.sel = b.sel;
+    a.pick_next = 0;
+    a.sel_next = b.sel[(l + 1) & 1];
+    a.hist_nn = nullptr;
+    a.sel = b.sel[l & 1];
     a.status = b.status;
     a.per_cta = 0;
     a.ld = p.ld;
@@ -769,7 +804,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 152;
-        const int64_t grid = (int64_t)sms * 8;  // eight partition CTAs per SM stay resident
+        const int64_t grid = (int64_t)sms * kPartCtas;  // partition CTAs stay resident
         a.per_cta = (live + grid - 1) / grid;
         const int64_t nblk = (live + a.per_cta - 1) / a.per_cta;
         const bool fused_here = l > 0 && fusable;
@@ -787,10 +822,17 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
             level_hist_kernel<<<(unsigned)nblk, kLvlThreads, hsm, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
-        {
+        // picks: by the level above's resolve when it could (this level's
+        // histograms were fused there), else by their own kernel; likewise
+        // this level's resolve picks for the next level
+        if (!fused_here) {
             ProfScope ps(stream, "pick", 0.0);
             level_pick_kernel<<<(unsigned)nseg, kPickThreads, 0, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
+        }
+        if (a.hist_nxt != nullptr && l + 1 < p.multi_levels) {
+            a.pick_next = 1;
+            if (l + 2 < p.finish_level) a.hist_nn = b.hist[l & 1];  // level l+2's rows, cleared for the grandchildren
         }
         {
             ProfScope ps(stream, "part", alg);
