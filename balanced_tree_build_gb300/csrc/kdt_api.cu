@@ -227,7 +227,7 @@ int kdt_build_host(const float *host_pts, int64_t N, int k, int split_mode, int3
             return KDT_ECUDA;
         pts_in = d_pts;
     }
-    rc = enqueue_build(p, b, pts_in, perm_out ? perm_out : d_perm, s);
+    rc = enqueue_build(p, b, pts_in, perm_out ? perm_out : d_perm, s, pts_in == d_pts);
     if (rc != KDT_OK) return rc;
     if (!perm_out && cudaMemcpyAsync(host_perm, d_perm, (size_t)N * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return KDT_ECUDA;

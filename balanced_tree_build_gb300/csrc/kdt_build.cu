@@ -132,8 +132,9 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
 }
 
 // k = 3, points 16-byte aligned: four points are three 128-bit loads, and two
-// such groups per thread are in flight at once.  Besides the records, the
-// first coordinate's keys go to a dense column (`col0`, may be null) that the
+// such groups per thread are in flight at once.  Besides the records (`rec`,
+// null when the first level reads the points itself), the first
+// coordinate's keys go to a dense column (`col0`, may be null) that the
 // first level's histogram reads instead of the 16-byte records.
 constexpr int kInit3Threads = 256;
 
@@ -185,8 +186,9 @@ __global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 init3_point(f[3 * i], f[3 * i + 1], f[3 * i + 2], (uint32_t)(4 * g + i), r[i], mn, mx, bad);
+            if (rec)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) rec[4 * g + i] = r[i];
+                for (int i = 0; i < 4; ++i) rec[4 * g + i] = r[i];
             if (col0) reinterpret_cast<uint4 *>(col0)[g] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
         }
     }
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__
     if (tail < N) {
         uint4 r;
         init3_point(pts[3 * tail], pts[3 * tail + 1], pts[3 * tail + 2], (uint32_t)tail, r, mn, mx, bad);
-        rec[tail] = r;
+        if (rec) rec[tail] = r;
         if (col0) col0[tail] = r.x;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
@@ -286,6 +288,7 @@ Buffers carve(const Plan &p, void *base) {
     r.bbox = reinterpret_cast<uint32_t *>(b + p.off_bbox);
     for (int i = 0; i < 3; ++i) r.rec[i] = reinterpret_cast<uint4 *>(b + p.off_rec[i]);
     r.col0 = nullptr;
+    r.pts3 = nullptr;
     for (int i = 0; i < 2; ++i) {
         r.dom[i] = reinterpret_cast<float *>(b + p.off_dom[i]);
         r.dim[i] = reinterpret_cast<int *>(b + p.off_dim[i]);
@@ -303,7 +306,8 @@ Buffers carve(const Plan &p, void *base) {
         if (e_ != cudaSuccess) return KDT_ECUDA;                \
     } while (0)
 
-int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t *perm, cudaStream_t stream) {
+int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t *perm, cudaStream_t stream,
+                  bool pts_in_hbm) {
     Buffers b = b_in;
     const Shape &S = p.S;
     const int k = p.k;
@@ -329,11 +333,16 @@ int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t 
             uint32_t *col0 = p.finish_level > 0 && p.mode == KDT_SPLIT_ROUND_ROBIN
                                  ? reinterpret_cast<uint32_t *>(b.rec[2]) : nullptr;
             b.col0 = col0;
+            // with the points in HBM, the first (multi-CTA, round-robin)
+            // level reads them directly and builds the records in registers:
+            // the 16-byte records are neither written here nor read there
+            if (pts_in_hbm && col0 && p.multi_levels > 0) b.pts3 = pts;
             int64_t g3 = (S.N / 4 + 2 * kInit3Threads - 1) / (2 * kInit3Threads);
             const int64_t cap3 = (int64_t)(sms > 0 ? sms : 152) * 16;
             if (g3 > cap3) g3 = cap3;
             if (g3 < 1) g3 = 1;
-            init3_kernel<<<(unsigned)g3, kInit3Threads, 0, stream>>>(pts, S.N, b.rec[0], col0, b.bbox, b.status);
+            init3_kernel<<<(unsigned)g3, kInit3Threads, 0, stream>>>(pts, S.N, b.pts3 ? nullptr : b.rec[0], col0,
+                                                                    b.bbox, b.status);
         } else if (k <= 3)
             init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);

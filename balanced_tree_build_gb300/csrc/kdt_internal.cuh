@@ -268,6 +268,7 @@ struct Buffers {
     uint32_t *bbox;  // [2k]: min keys then max keys
     uint4 *rec[3];   // record buffers: [0], [1] ping-pong, [2] bucket candidates
     const uint32_t *col0;  // dense keys of coordinate 0 for the first level's histogram, or null
+    const float *pts3;     // k = 3 input points that the first level reads in place of records, or null
     float *dom[2];   // node tables: entry e holds lo[k] then hi[k]
     int *dim[2];
     uint32_t *hist[2];  // [rows][kBuckets]
@@ -291,8 +292,10 @@ int launch_select_finisher(const Plan &p, const Buffers &b, int src, int32_t *pe
 int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm, cudaStream_t stream);
 
 // Enqueues the whole build on `stream`.  Returns a KDT_* code for launch errors.
+// `pts_in_hbm`: pts is device memory (not host memory mapped into the
+// device's address space), so reading it twice costs HBM bandwidth only.
 int enqueue_build(const Plan &p, const Buffers &b, const float *pts, int32_t *perm,
-                  cudaStream_t stream);
+                  cudaStream_t stream, bool pts_in_hbm = true);
 
 // Per-kernel timing (profiling switch in kdt_api.cu).  `kernels`: kernel
 // launches inside the scope (1 unless the code between the events says so).

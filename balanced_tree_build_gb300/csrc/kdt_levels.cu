@@ -32,6 +32,8 @@
 namespace kdt {
 
 constexpr int kLvlThreads = 512;
+constexpr int kResThreadsMax = 1024;  // resolve CTAs of subtrees with many candidates
+constexpr uint32_t kSelList = 2048;   // listed candidates of a resolve CTA's select
 constexpr int kPickThreads = 256;
 constexpr int kEPT = 4;                          // consecutive points per thread per tile (divides 8: rows up to
                                                  // the next multiple of 8 exist in every record buffer)
@@ -135,6 +137,10 @@ struct LevelArgs {
     int hist_in;         // per-subtree levels: this level's histograms were built by the level above
     int warp_res;        // partition: each warp reserves its own output ranges (no CTA barriers)
     const uint32_t *col0;  // level 0, round-robin: dense keys of the split coordinate (else null)
+    // level 0, k = 3: the input points (16-byte aligned float triples, point q
+    // at position q), read in place of the records, which are built in
+    // registers (else null)
+    const float *pts3;
     // resolve: pick the next level's split buckets for this subtree's two
     // children (their histograms are final once its candidates are added)
     int pick_next;
@@ -218,6 +224,13 @@ struct PartPlan {
 // into L2, so that the tile's loads, issued two tiles later, wait on L2
 // rather than DRAM: one 128-byte line (8 records) per thread and group.
 __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve) {
+    if (a.pts3 != nullptr) {  // the tile's float triples: 12 bytes per point
+        const char *p = reinterpret_cast<const char *>(a.pts3);
+        const int64_t b0 = 12 * t0, b1 = 12 * min(ve, t0 + (int64_t)kTile);
+        for (int64_t o = b0 + 128 * (int64_t)threadIdx.x; o < b1; o += 128 * (int64_t)blockDim.x)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+        return;
+    }
     const uint32_t lines = kTile / 8;  // 128-byte lines per group column
     for (uint32_t t = threadIdx.x; t < (uint32_t)a.G * lines; t += blockDim.x) {
         const uint32_t gi = t / lines;
@@ -253,8 +266,29 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     // group 0 of the thread's four records (for k <= 3 the whole record);
     // rows up to q0 + 3 < ld exist in every buffer
     uint4 r[kEPT];
+    if (a.pts3 != nullptr) {  // level 0, k = 3: four points are three 128-bit words of the input
+        if (any && q0 + (uint32_t)kEPT <= (uint32_t)a.S.N) {
+            const uint4 *p4 = reinterpret_cast<const uint4 *>(a.pts3) + 3u * (q0 >> 2);
+            const uint4 v0 = __ldg(p4), v1 = __ldg(p4 + 1), v2 = __ldg(p4 + 2);
+            const uint32_t f[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
 #pragma unroll
-    for (int i = 0; i < kEPT; ++i) r[i] = any ? __ldg(a.src + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < kEPT; ++i)
+                r[i] = make_uint4(f2key(__uint_as_float(f[3 * i])), f2key(__uint_as_float(f[3 * i + 1])),
+                                  f2key(__uint_as_float(f[3 * i + 2])), q0 + (uint32_t)i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kEPT; ++i) {
+                const uint32_t q = q0 + (uint32_t)i;
+                r[i] = any && q < (uint32_t)a.S.N
+                           ? make_uint4(f2key(__ldg(a.pts3 + 3u * q)), f2key(__ldg(a.pts3 + 3u * q + 1u)),
+                                        f2key(__ldg(a.pts3 + 3u * q + 2u)), q)
+                           : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i) r[i] = any ? __ldg(a.src + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
     uint32_t kx[kEPT];
 #pragma unroll
     for (int i = 0; i < kEPT; ++i)
@@ -386,7 +420,8 @@ struct CandAcc {
 // gap between the certain groups.  `fuse`: add the candidates to the
 // children's histograms of the next level.
 __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const PartPlan &pp, SelState &st,
-                                uint32_t *hist, uint32_t *red, uint32_t *medw, uint32_t *cur2, bool fuse, int dn) {
+                                uint32_t *hist, uint32_t *red, uint32_t *medw, uint32_t *cur2, bool fuse, int dn,
+                                uint32_t *qbuf, uint32_t qcap) {
     const uint32_t tid = threadIdx.x, nt = blockDim.x;
     const int k = a.k;
     const int64_t ld = a.ld;
@@ -396,7 +431,7 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
         if (tid < 32u) group_select(WarpsGroup{0u, 32u, 1}, acc, pp.cnt, r, k + 1, st, hist, kWarpRadixBits, red);
         __syncthreads();
     } else {
-        cta_select(acc, pp.cnt, r, k + 1, st, hist, red);
+        cta_select(acc, pp.cnt, r, k + 1, st, hist, red, qbuf, qcap);
     }
     if (st.err) {
         if (tid == 0) set_status(a.status, KDT_EINTERNAL);
@@ -656,9 +691,10 @@ __global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(Lev
     }
 }
 
-__global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a) {
+__global__ void __launch_bounds__(kResThreadsMax) level_resolve_kernel(LevelArgs a) {
     __shared__ SelState st;
     __shared__ uint32_t hist[kCtaRadixBins];
+    __shared__ uint32_t qbuf[kSelList];
     __shared__ uint32_t red[64];
     __shared__ uint32_t medw[kMaxWords];
     __shared__ uint32_t cur2[2];
@@ -672,7 +708,7 @@ __global__ void __launch_bounds__(kLvlThreads) level_resolve_kernel(LevelArgs a)
         if (threadIdx.x == 0) set_status(a.status, KDT_EINTERNAL);
         return;
     }
-    resolve_segment(a, g, pp, st, hist, red, medw, cur2, a.hist_nxt != nullptr, (a.l + 1) % a.k);
+    resolve_segment(a, g, pp, st, hist, red, medw, cur2, a.hist_nxt != nullptr, (a.l + 1) % a.k, qbuf, kSelList);
     if (a.pick_next && !st.err) {
         // the children's histograms are final now (the part pass flushed its
         // counts before this kernel; this CTA added the candidates'), and so
@@ -760,7 +796,9 @@ __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a)
         for (uint32_t b = threadIdx.x; b < 2u * kBuckets; b += blockDim.x) H[b] = fh[b];
         __syncthreads();  // before the resolve adds the candidates to the same rows
     }
-    resolve_segment(a, g, pp, st, hist, red, medw, cur2, fuse, dn);
+    // fh is free again (written out above, or unused): the select lists its
+    // last candidates there
+    resolve_segment(a, g, pp, st, hist, red, medw, cur2, fuse, dn, fh, 2u * kBuckets);
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -788,6 +826,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.hist_in = 0;
     a.warp_res = 0;  // multi-CTA levels: one global reservation per CTA and tile
     a.col0 = l == 0 ? b.col0 : nullptr;
+    a.pts3 = l == 0 && l < p.multi_levels ? b.pts3 : nullptr;
     a.pick_next = 0;
     a.sel_next = b.sel[(l + 1) & 1];
     a.hist_nn = nullptr;
@@ -841,7 +880,10 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         }
         {
             ProfScope ps(stream, "resolve", 0.0);
-            level_resolve_kernel<<<(unsigned)nseg, kLvlThreads, 0, stream>>>(a);
+            // many candidates per subtree (the top levels): a wider CTA
+            const double cand = (double)live / (double)nseg / (double)(l == 0 ? kBuckets0 : kBuckets);
+            const int rt = cand > 4096.0 ? kResThreadsMax : kLvlThreads;
+            level_resolve_kernel<<<(unsigned)nseg, rt, 0, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
     } else {

@@ -44,6 +44,8 @@ struct SelState {
     float vlo, vscale;
     uint32_t med_q;         // result: position of the selected point
     int err;
+    int listed;             // the matching points' positions are listed in the group's buffer
+    uint32_t nq;            // entries of that list
 };
 
 // ---- thread groups ------------------------------------------------------------
@@ -136,12 +138,13 @@ __device__ __forceinline__ uint32_t value_bucket(uint32_t key, float lo, float s
 }
 
 // Calls f(q, word j of q) for every matching point q of the group's share of
-// [0, n).  Word 0 of eight points is loaded before any of them is tested, so
-// a thread keeps eight loads in flight (the points may sit in global memory);
-// the other words are read only for points that still match.
+// [0, n), or of the list `qlist` once the matching points were listed there.
+// Word 0 of eight points is loaded before any of them is tested, so a thread
+// keeps eight loads in flight (the points may sit in global memory); the
+// other words are read only for points that still match.
 template <class G, class Acc, class F>
 __device__ __forceinline__ void for_matching(const G &g, const Acc &acc, const SelState &st, uint32_t n, uint32_t nb,
-                                             F f) {
+                                             const uint32_t *qlist, F f) {
     constexpr int kB = 8;
     const uint32_t tid = g.tid(), nt = g.size();
     const int j = st.j;
@@ -154,6 +157,13 @@ __device__ __forceinline__ void for_matching(const G &g, const Acc &acc, const S
         if (st.has_prefix && (wj >> st.sh) != st.pv) return;
         f(q, wj);
     };
+    if (st.listed) {
+        for (uint32_t i = tid; i < st.nq; i += nt) {
+            const uint32_t q = qlist[i];
+            test(q, acc(0, q));
+        }
+        return;
+    }
     if (n <= nt) {  // at most one point per thread: nothing to batch
         if (tid < n) test(tid, acc(0, tid));
         return;
@@ -185,12 +195,15 @@ __device__ __forceinline__ int cmp_words(const Acc &acc, uint32_t q, const uint3
 
 // Group-wide exact select of rank m among n points (positions 0..n-1 through
 // `acc`).  `hist` holds 2^bits words (2^bits a multiple of the group size),
-// `red` >= 64 words, `st` is the group's state; all in shared memory.  On
-// return (after a group barrier) st.med_q holds the selected position and
-// st.err is nonzero on an internal inconsistency.
+// `red` >= 64 words, `st` is the group's state; all in shared memory.  With a
+// list buffer (`qbuf`, `qcap` words of shared memory, or null), once at most
+// qcap points still match they are listed there, and the later rounds visit
+// only those instead of all n.  On return (after a group barrier) st.med_q
+// holds the selected position and st.err is nonzero on an internal
+// inconsistency.
 template <class G, class Acc>
 __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m, int nwords, SelState &st,
-                             uint32_t *hist, int bits, uint32_t *red) {
+                             uint32_t *hist, int bits, uint32_t *red, uint32_t *qbuf = nullptr, uint32_t qcap = 0u) {
     const uint32_t tid = g.tid(), nt = g.size();
     const uint32_t nbins = 1u << bits;
     if (tid == 0) {
@@ -206,6 +219,8 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
         st.vscale = 0.f;
         st.err = 0;
         st.med_q = 0;
+        st.listed = 0;
+        st.nq = 0;
     }
     g.sync();
     bool value_round = true;
@@ -213,7 +228,7 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
         if (st.cnt <= 1u || st.j >= nwords) break;
         const int j = st.j;
         uint32_t mn = 0xffffffffu, mx = 0u;
-        for_matching(g, acc, st, n, nbins, [&](uint32_t, uint32_t w) {
+        for_matching(g, acc, st, n, nbins, qbuf, [&](uint32_t, uint32_t w) {
             mn = min(mn, w);
             mx = max(mx, w);
         });
@@ -250,7 +265,7 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
         }
         for (uint32_t b = tid; b < nbins; b += nt) hist[b] = 0u;
         g.sync();
-        for_matching(g, acc, st, n, nbins, [&](uint32_t, uint32_t w) {
+        for_matching(g, acc, st, n, nbins, qbuf, [&](uint32_t, uint32_t w) {
             const uint32_t b = vround ? value_bucket(w, vlo, vscale, nbins) : (w >> sh) - lo;
             atomicAdd(&hist[b], 1u);
         });
@@ -291,18 +306,35 @@ __device__ void group_select(const G &g, const Acc &acc, uint32_t n, uint32_t m,
             }
         }
         g.sync();
+        // few points left of many: list them once
+        if (qbuf != nullptr && !st.listed && st.cnt > 1u && st.cnt <= qcap && n > 2u * nt) {
+            for_matching(g, acc, st, n, nbins, qbuf, [&](uint32_t q, uint32_t) {
+                const uint32_t i = atomicAdd(&st.nq, 1u);
+                if (i < qcap) qbuf[i] = q;
+            });
+            g.sync();
+            if (tid == 0) {
+                if (st.nq != st.cnt) {
+                    st.err = 1;
+                    st.cnt = 0u;  // ends the loop
+                }
+                st.listed = 1;
+            }
+            g.sync();
+        }
     }
     if (st.cnt != 1u && tid == 0) st.err = 1;
     g.sync();
-    for_matching(g, acc, st, n, nbins, [&](uint32_t q, uint32_t) { st.med_q = q; });
+    for_matching(g, acc, st, n, nbins, qbuf, [&](uint32_t q, uint32_t) { st.med_q = q; });
     g.sync();
 }
 
 // CTA-wide select with 2^11 buckets (global levels).
 template <class Acc>
 __device__ __forceinline__ void cta_select(const Acc &acc, uint32_t n, uint32_t m, int nwords, SelState &st,
-                                           uint32_t *hist, uint32_t *red) {
-    group_select(CtaGroup{}, acc, n, m, nwords, st, hist, kCtaRadixBits, red);
+                                           uint32_t *hist, uint32_t *red, uint32_t *qbuf = nullptr,
+                                           uint32_t qcap = 0u) {
+    group_select(CtaGroup{}, acc, n, m, nwords, st, hist, kCtaRadixBits, red, qbuf, qcap);
 }
 
 }  // namespace kdt
