@@ -77,10 +77,11 @@ static size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 // buckets (after the sort: the node tables of a level), a [T] u16 bucket
 // staging array (after the sort, in widest mode: the split dimension of each
 // node of a level), and in widest mode the split value and dimension of
-// every tile node.
+// every tile node, in round-robin mode with k = 3 a segment code per point.
 size_t sorted_finisher_smem(int k, int T, int mode, int nb) {
     size_t b = (size_t)2 * k * T + (size_t)4 * k * T + (size_t)4 * T + (size_t)nb + (size_t)nb / 2 + (size_t)2 * T;
     if (mode == KDT_SPLIT_WIDEST) b += (size_t)5 * T;
+    else if (k == 3) b += (size_t)T;  // segment code per point (k = 3 schedule)
     return align16(b);
 }
 
@@ -96,6 +97,7 @@ struct SfSmem {
     uint8_t *ldim;    // [T/2] split dimension per node of a level, aliases stage (widest mode)
     float *sval;      // [T] split value of tile node (widest mode)
     uint8_t *sdim;    // [T] split dimension of tile node (widest mode)
+    uint8_t *segtab;  // [T] segment code per point on the first two levels (k = 3 round-robin), aliases sval
 };
 
 __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int nb) {
@@ -115,6 +117,7 @@ __device__ __forceinline__ SfSmem sf_carve(unsigned char *p, int k, int T, int n
     f.ldim = p;
     p += (size_t)2 * T;
     f.sval = reinterpret_cast<float *>(p);
+    f.segtab = p;
     p += (size_t)4 * T;
     f.sdim = p;
     return f;
@@ -268,6 +271,148 @@ __device__ __forceinline__ void sf_block_minmax(uint32_t &mn, uint32_t &mx, uint
     __syncthreads();
 }
 
+// Orders the local ids 0..n-1 into arr = ids[c] by the super key of
+// coordinate c: a counting sort into value buckets of x[c] (a monotone map of
+// its key), then each point's rank inside its bucket by comparison under the
+// full super key.  With nseg > 1 the points are split into segments first:
+// code[q] < nseg is point q's segment, code[q] = 4 + j marks a point that
+// already has its position fxp[j]; the buckets are taken per segment (nb /
+// nseg each), and a point of segment g that is r-th among the other points
+// in (segment, bucket, rank) order goes to position r + g -- the segments are
+// the subtrees of consecutive in-order ranges, one fixed point between each
+// two.  Returns false (in every thread) if a bucket holds more than
+// kSfMaxBucket points: the tile is then left to the select finisher (or, for
+// a balanced tile, which has none, the coordinate is sorted outright).
+template <int NT>
+__device__ bool sort_coord(const SfSmem &sm, uint32_t *red, int T, int k, int nb, uint32_t n, int c, int nseg,
+                           const uint8_t *code, const uint32_t *fxp, bool bal) {
+    constexpr int NW = NT / 32, E = kSfPPT;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t tmask0 = (uint32_t)T - 1u;  // positions stay inside the tile's arrays
+    const uint32_t *kc = sm.keys + c * T;
+    uint16_t *arr = sm.ids + c * T;
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (uint32_t q = tid; q < n; q += NT) {
+        const uint32_t v = kc[q];
+        mn = min(mn, v);
+        mx = max(mx, v);
+    }
+    sf_block_minmax<NW>(mn, mx, red);
+    const uint32_t nbs = (uint32_t)nb / (uint32_t)nseg;  // buckets per segment (powers of two)
+    const int lgs = 31 - __clz((int)nbs);
+    const float lo = key2f(mn);
+    const float rg = __fsub_rn(key2f(mx), lo);
+    float scale = 0.f;
+    bool spread = false;
+    if (mn != mx && rg > 0.f && rg <= 3.0e38f) {
+        scale = __fdiv_rn((float)nbs, rg);
+        spread = scale > 0.f && scale <= 3.0e38f;
+    }
+    if (!spread && n > (uint32_t)kSfMaxBucket) {  // same decision in every thread
+        if (bal && nseg == 1) {  // balanced tiles have no select fallback: sort this coordinate outright
+            bitonic_sort_ids<NT>(arr, kc, sm.keys, sm.idx, T, k, c, n);
+            return true;
+        }
+        return false;
+    }
+    for (uint32_t b = tid; b < (uint32_t)nb / 4u; b += NT) sm.hist[b] = 0u;
+    __syncthreads();
+    // bucket and arrival slot of each held point (8-bit counters: a slot of
+    // kSfMaxBucket or more gives up before any counter can carry into its
+    // neighbour); a point with its position already fixed is not counted
+    uint32_t pk[E];
+    int big = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const uint32_t q = tid + (uint32_t)i * NT;
+        pk[i] = 0xffffffffu;
+        if (q < n) {
+            uint32_t g = 0u;
+            if (nseg > 1) {
+                g = code[q];
+                if (g >= 4u) continue;
+            }
+            const uint32_t b = (g << lgs) + (spread ? value_bucket(kc[q], lo, scale, nbs) : 0u);
+            const uint32_t sh = (b & 3u) << 3;
+            const uint32_t r = (atomicAdd(&sm.hist[b >> 2], 1u << sh) >> sh) & 0xffu;
+            big |= r >= (uint32_t)kSfMaxBucket;
+            pk[i] = (b << 16) | r;
+        }
+    }
+    if (__syncthreads_or(big)) {
+        if (bal && nseg == 1) {
+            bitonic_sort_ids<NT>(arr, kc, sm.keys, sm.idx, T, k, c, n);
+            return true;
+        }
+        return false;
+    }
+    // exclusive scan of the counts: four counter words (16 buckets) per
+    // thread; the first position of each word's buckets goes to base16
+    constexpr uint32_t WPT = 4;  // nb / 4 / NT with nb = 2T = 16 NT
+    uint32_t hw[WPT], sum = 0u;
+#pragma unroll
+    for (uint32_t i = 0; i < WPT; ++i) {
+        hw[i] = sm.hist[tid * WPT + i];
+        sum += (hw[i] * 0x01010101u) >> 24;  // byte sum (each count <= kSfMaxBucket)
+    }
+    uint32_t run = block_exclusive_scan(sum, red);
+#pragma unroll
+    for (uint32_t i = 0; i < WPT; ++i) {
+        sm.base16[tid * WPT + i] = (uint16_t)run;
+        run += (hw[i] * 0x01010101u) >> 24;
+    }
+    __syncthreads();
+    // group the points by bucket; st = first position | size << 16
+    uint32_t st[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const uint32_t q = tid + (uint32_t)i * NT;
+        st[i] = 0u;
+        if (pk[i] != 0xffffffffu) {
+            const uint32_t b = pk[i] >> 16, j8 = (b & 3u) << 3;
+            const uint32_t wv = sm.hist[b >> 2];
+            const uint32_t beg = sm.base16[b >> 2] + (((wv * 0x01010100u) >> j8) & 0xffu);  // bytes below b
+            sm.stage[(beg + (pk[i] & 0xffffu)) & tmask0] = (uint16_t)q;
+            st[i] = beg | (((wv >> j8) & 0xffu) << 16);
+        }
+    }
+    __syncthreads();
+    // rank inside the bucket under the super key of c; the held points step
+    // through their buckets together, so their loads overlap
+    uint32_t kq[E], rank[E], smax = 0u;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const uint32_t q = tid + (uint32_t)i * NT;
+        const uint32_t sz = st[i] >> 16;
+        rank[i] = 0u;
+        kq[i] = sz > 1u ? kc[q] : 0u;
+        if (sz > 1u) smax = max(smax, sz);
+    }
+    for (uint32_t j = 0; j < smax; ++j) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const uint32_t sz = st[i] >> 16;
+            if (j < sz && sz > 1u) {
+                const uint32_t q = tid + (uint32_t)i * NT;
+                const uint32_t o = sm.stage[((st[i] & 0xffffu) + j) & tmask0];
+                const uint32_t ko = kc[o];
+                rank[i] += (ko < kq[i] || (ko == kq[i] && o != q && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q)))
+                               ? 1u
+                               : 0u;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const uint32_t q = tid + (uint32_t)i * NT;
+        if (q >= n) continue;
+        if (pk[i] != 0xffffffffu) arr[((st[i] & 0xffffu) + rank[i] + ((pk[i] >> 16) >> lgs)) & tmask0] = (uint16_t)q;
+        else arr[fxp[min(code[q] - 4u, 2u)] & tmask0] = (uint16_t)q;  // nseg > 1: a fixed point
+    }
+    __syncthreads();
+    return true;
+}
+
 // Segmented sum: `cur` continues the range of `prev` unless a range starts in
 // it (kSegHead); the flag of either side survives in bit 31 (values < 2^29).
 __device__ __forceinline__ uint32_t seg_combine(uint32_t prev, uint32_t cur) {
@@ -290,6 +435,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     __shared__ uint32_t red[64];
     __shared__ uint32_t wagg[2][NW];  // [round parity][warp]: segmented warp sums
     __shared__ uint64_t wagg64[NW];   // k = 3 schedule: segmented warp sums of the 4-field scan
+    __shared__ uint32_t fxp[3];      // k = 3 schedule: in-order positions of the tile root and its children
     __shared__ int stop;
     const uint32_t tid = threadIdx.x;
     const uint32_t w = tid >> 5, lane = tid & 31u;
@@ -337,124 +483,18 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     }
     __syncthreads();
 
-    // 2. one reference array per coordinate, sorted by its super key
-    const uint32_t tmask0 = (uint32_t)T - 1u;  // positions stay inside the tile's arrays
+    // 2. one reference array per coordinate, sorted by its super key (the
+    //    k = 3 schedule of a left-balanced tile: only the tile root's split
+    //    coordinate here; the next two are sorted per subtree on levels 0
+    //    and 1, when the splits above them are known)
+    const bool segs = K3 && !bal;
     bool fail = false;
     for (int c = 0; c < k; ++c) {
-        const uint32_t *kc = sm.keys + c * T;
-        uint32_t mn = 0xffffffffu, mx = 0u;
-        for (uint32_t q = tid; q < n; q += NT) {
-            const uint32_t v = kc[q];
-            mn = min(mn, v);
-            mx = max(mx, v);
-        }
-        sf_block_minmax<NW>(mn, mx, red);
-        const float lo = key2f(mn);
-        const float rg = __fsub_rn(key2f(mx), lo);
-        float scale = 0.f;
-        bool spread = false;
-        if (mn != mx && rg > 0.f && rg <= 3.0e38f) {
-            scale = __fdiv_rn((float)nb, rg);
-            spread = scale > 0.f && scale <= 3.0e38f;
-        }
-        if (!spread && n > (uint32_t)kSfMaxBucket) {  // same decision in every thread
-            if (bal) {  // balanced tiles have no select fallback: sort this coordinate outright
-                bitonic_sort_ids<NT>(sm.ids + c * T, kc, sm.keys, sm.idx, T, k, c, n);
-                continue;
-            }
+        if (segs && c != a.l0 % 3) continue;
+        if (!sort_coord<NT>(sm, red, T, k, nb, n, c, 1, nullptr, nullptr, bal)) {
             fail = true;
             break;
         }
-        for (uint32_t b = tid; b < (uint32_t)nb / 4u; b += NT) sm.hist[b] = 0u;
-        __syncthreads();
-        // bucket and arrival slot of each held point (8-bit counters: a slot
-        // of kSfMaxBucket or more leaves the tile to the select finisher,
-        // before any counter can carry into its neighbour)
-        uint32_t pk[E];
-        int big = 0;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const uint32_t q = tid + (uint32_t)i * NT;
-            pk[i] = 0u;
-            if (q < n) {
-                const uint32_t b = spread ? value_bucket(kc[q], lo, scale, (uint32_t)nb) : 0u;
-                const uint32_t sh = (b & 3u) << 3;
-                const uint32_t r = (atomicAdd(&sm.hist[b >> 2], 1u << sh) >> sh) & 0xffu;
-                big |= r >= (uint32_t)kSfMaxBucket;
-                pk[i] = (b << 16) | r;
-            }
-        }
-        if (__syncthreads_or(big)) {
-            if (bal) {
-                bitonic_sort_ids<NT>(sm.ids + c * T, kc, sm.keys, sm.idx, T, k, c, n);
-                continue;
-            }
-            fail = true;
-            break;
-        }
-        // exclusive scan of the counts: four counter words (16 buckets) per
-        // thread; the first position of each word's buckets goes to base16
-        constexpr uint32_t WPT = 4;  // nb / 4 / NT with nb = 2T = 16 NT
-        uint32_t hw[WPT], sum = 0u;
-#pragma unroll
-        for (uint32_t i = 0; i < WPT; ++i) {
-            hw[i] = sm.hist[tid * WPT + i];
-            sum += (hw[i] * 0x01010101u) >> 24;  // byte sum (each count <= kSfMaxBucket)
-        }
-        uint32_t run = block_exclusive_scan(sum, red);
-#pragma unroll
-        for (uint32_t i = 0; i < WPT; ++i) {
-            sm.base16[tid * WPT + i] = (uint16_t)run;
-            run += (hw[i] * 0x01010101u) >> 24;
-        }
-        __syncthreads();
-        // group the points by bucket; st = first position | size << 16
-        uint32_t st[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const uint32_t q = tid + (uint32_t)i * NT;
-            st[i] = 0u;
-            if (q < n) {
-                const uint32_t b = pk[i] >> 16, j8 = (b & 3u) << 3;
-                const uint32_t wv = sm.hist[b >> 2];
-                const uint32_t beg = sm.base16[b >> 2] + (((wv * 0x01010100u) >> j8) & 0xffu);  // bytes below b
-                sm.stage[(beg + (pk[i] & 0xffffu)) & tmask0] = (uint16_t)q;
-                st[i] = beg | (((wv >> j8) & 0xffu) << 16);
-            }
-        }
-        __syncthreads();
-        // rank inside the bucket under the super key of c; the held points
-        // step through their buckets together, so their loads overlap
-        uint16_t *arr = sm.ids + c * T;
-        uint32_t kq[E], rank[E], smax = 0u;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const uint32_t q = tid + (uint32_t)i * NT;
-            const uint32_t sz = st[i] >> 16;
-            rank[i] = 0u;
-            kq[i] = sz > 1u ? kc[q] : 0u;
-            if (sz > 1u) smax = max(smax, sz);
-        }
-        for (uint32_t j = 0; j < smax; ++j) {
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                const uint32_t sz = st[i] >> 16;
-                if (j < sz && sz > 1u) {
-                    const uint32_t q = tid + (uint32_t)i * NT;
-                    const uint32_t o = sm.stage[((st[i] & 0xffffu) + j) & tmask0];
-                    const uint32_t ko = kc[o];
-                    rank[i] += (ko < kq[i] || (ko == kq[i] && o != q && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q)))
-                                   ? 1u
-                                   : 0u;
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const uint32_t q = tid + (uint32_t)i * NT;
-            if (q < n) arr[((st[i] & 0xffffu) + rank[i]) & tmask0] = (uint16_t)q;
-        }
-        __syncthreads();
     }
     if (tid == 0) a.fallback[tile] = fail ? 1 : 0;
     if (fail) return;
@@ -475,14 +515,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     const uint32_t Mt = n - ((1u << (h - 1)) - 1u);
     const uint32_t p0 = tid * (uint32_t)E;
     const bool wact = w * 32u * (uint32_t)E < n;  // the warp holds a position of the tile
+    // the left-aligned code of the node at in-order position p (0 past the tile)
+    auto gcode = [&](uint32_t p) -> uint32_t {
+        const uint32_t u1 = p < n ? tile_node1(bal, p, h, Mt, n) : 0u;
+        return u1 ? ((u1 << 1) | 1u) << (__clz((int)u1) - 1) : 0u;
+    };
     uint32_t g[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const uint32_t u1 = p0 + e < n ? tile_node1(bal, p0 + e, h, Mt, n) : 0u;
-        g[e] = u1 ? ((u1 << 1) | 1u) << (__clz((int)u1) - 1) : 0u;
-    }
-    uint32_t gprev = (p0 > 0u && p0 - 1u < n) ? tile_node1(bal, p0 - 1u, h, Mt, n) : 0u;
-    gprev = gprev ? ((gprev << 1) | 1u) << (__clz((int)gprev) - 1) : 0u;
     const int last = h - 2;  // deepest level that moves an array
     if (!rr) {
         if (tid == 0) sm.ldim[0] = (uint8_t)sf_widest_dim(a, sm, s0, 0, 0);
@@ -505,12 +543,64 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         uint16_t *side16 = reinterpret_cast<uint16_t *>(sm.side);
         uint16_t *ptab0 = reinterpret_cast<uint16_t *>(sm.ntab);   // [T/2] in-order position + 1 of each node of a level
         uint16_t *ptab1 = ptab0 + T / 2;
-        int dl = a.l0 % 3;
-        for (int l = 0; l < last; ++l, dl = dl == 2 ? 0 : dl + 1) {
+        // Left-balanced tiles sort d_1 and d_2 per subtree instead (levels 0
+        // and 1 below): the segment code of each point (its side of the
+        // splits above, or which split point it is) goes to segtab, and the
+        // sort puts every point at its position for the next level directly.
+        int l_first = 0;
+        if (segs) {
+            if (tid < 3u)
+                fxp[tid] = tid == 0u ? tile_pos(bal, 0u, 0, h, Mt, n) : (h >= 2 ? tile_pos(bal, tid - 1u, 1, h, Mt, n) : 0u);
+            for (int l = 0; l < last && l < 2; ++l) {
+                const int dl = (a.l0 + l) % 3, c = (a.l0 + l + 1) % 3;  // d_l, d_{l+1}
+                // A': segment codes from d_l -- level 0: 0 left, 1 right, 4
+                //     the root; level 1: 2 * (level-0 side) + side, 5 / 6 the
+                //     split points of the root's children
+                if (wact) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sm.ids + dl * T + p0);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const uint32_t ge = gcode(p0 + (uint32_t)e);
+                        const uint32_t t = ge << (l + 1);
+                        if (t == 0u) continue;
+                        const uint32_t id = ids_at(v, e) & tmask;
+                        if (l == 0) sm.segtab[id] = (uint8_t)(t == 0x80000000u ? 4u : (t >> 31));
+                        else
+                            sm.segtab[id] = (uint8_t)(t == 0x80000000u ? 5u + ((ge >> 30) & 1u)
+                                                                        : 2u * sm.segtab[id] + (t >> 31));
+                    }
+                }
+                __syncthreads();
+                if (!sort_coord<NT>(sm, red, T, k, nb, n, c, 2 << l, sm.segtab, fxp, bal)) {
+                    if (tid == 0) a.fallback[tile] = 1;  // crowded: the select finisher takes the tile
+                    return;
+                }
+                if (l == 1) {
+                    // the keys are no longer read: level 1's sides go to the
+                    // side words for level 2's moves (the root is not looked up)
+                    for (uint32_t id = tid; id < n; id += NT) {
+                        const uint32_t cd = sm.segtab[id];
+                        if (cd == 4u) continue;
+                        side16[2u * id + 1u] = (uint16_t)(cd >= 5u ? (0x8000u | fxp[min(cd - 4u, 2u)]) : (cd & 1u));
+                    }
+                    __syncthreads();
+                }
+                l_first = l + 1;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) g[e] = gcode(p0 + (uint32_t)e);
+        const uint32_t gprev = p0 > 0u ? gcode(p0 - 1u) : 0u;
+        int dl = (a.l0 + l_first) % 3;
+        for (int l = l_first; l < last; ++l, dl = dl == 2 ? 0 : dl + 1) {
             const uint32_t q = (uint32_t)l & 1u;
             uint16_t *pt_l = q ? ptab1 : ptab0;
             const uint16_t *pt_p = q ? ptab0 : ptab1;  // level l - 1
+            const int c = dl == 2 ? 0 : dl + 1;  // d_{l+1}
             for (uint32_t i = tid; i < (1u << l); i += NT) pt_l[i] = (uint16_t)(tile_pos(bal, i, l, h, Mt, n) + 1u);
+            if (segs && l == 2) {  // level 1's table was overwritten by the sort's counters
+                for (uint32_t i = tid; i < 2u; i += NT) ptab1[i] = (uint16_t)(fxp[1u + i] + 1u);
+            }
             // A: side of every point of a level-l node, from d_l: 0 left,
             //    1 right, 0x8000 | position for the node's split point
             if (wact) {
@@ -524,7 +614,6 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                 }
             }
             __syncthreads();
-            const int c = dl == 2 ? 0 : dl + 1;  // d_{l+1}
             // B: live positions of level l-1 (level 0: the whole tile), running
             //    value before each held point, warp scan
             uint4 iv = make_uint4(0u, 0u, 0u, 0u);
@@ -604,6 +693,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
             __syncthreads();
         }
     } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) g[e] = gcode(p0 + (uint32_t)e);
+        const uint32_t gprev = p0 > 0u ? gcode(p0 - 1u) : 0u;
         const uint32_t allk = k >= 32 ? 0xffffffffu : (1u << k) - 1u;  // k <= KDT_MAX_K = 32
         int dl0 = rr ? a.l0 % k : 0;           // round-robin split coordinate of level l
         int par = 0;

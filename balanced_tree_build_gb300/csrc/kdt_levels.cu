@@ -223,8 +223,8 @@ struct PartPlan {
 // Prefetches the record lines of the tile starting at t0 (clipped to ve)
 // into L2, so that the tile's loads, issued two tiles later, wait on L2
 // rather than DRAM: one 128-byte line (8 records) per thread and group.
-__device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve) {
-    if (a.pts3 != nullptr) {  // the tile's float triples: 12 bytes per point
+__device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, int64_t ve, bool pts3 = false) {
+    if (pts3) {  // the tile's float triples: 12 bytes per point
         const char *p = reinterpret_cast<const char *>(a.pts3);
         const int64_t b0 = 12 * t0, b1 = 12 * min(ve, t0 + (int64_t)kTile);
         for (int64_t o = b0 + 128 * (int64_t)threadIdx.x; o < b1; o += 128 * (int64_t)blockDim.x)
@@ -251,6 +251,7 @@ __device__ __forceinline__ void prefetch_tile(const LevelArgs &a, int64_t t0, in
 // latency per tile.  Output order is slot-major per warp: for each of the 4
 // slots the warp's lanes going to one side write consecutive positions
 // (ballot + popcount), so every warp store covers one contiguous run.
+template <bool kPts3 = false>
 __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &bk, const PartPlan &pp, int64_t t0,
                           int64_t vb, int64_t ve, uint32_t *cursors, uint32_t *wtot, uint32_t *wbase, uint32_t *fh,
                           const Bucketer &bkc, int dn) {
@@ -266,7 +267,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
     // group 0 of the thread's four records (for k <= 3 the whole record);
     // rows up to q0 + 3 < ld exist in every buffer
     uint4 r[kEPT];
-    if (a.pts3 != nullptr) {  // level 0, k = 3: four points are three 128-bit words of the input
+    if constexpr (kPts3) {  // level 0, k = 3: four points are three 128-bit words of the input
         if (any && q0 + (uint32_t)kEPT <= (uint32_t)a.S.N) {
             const uint4 *p4 = reinterpret_cast<const uint4 *>(a.pts3) + 3u * (q0 >> 2);
             const uint4 v0 = __ldg(p4), v1 = __ldg(p4 + 1), v2 = __ldg(p4 + 2);
@@ -652,6 +653,8 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
     return pp;
 }
 
+// kPts3: level 0 reads the k = 3 input points in place of records (a.pts3).
+template <bool kPts3>
 __global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(LevelArgs a) {
     __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
@@ -677,8 +680,8 @@ __global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(Lev
         }
         __syncthreads();
         for (int64_t t0 = p & ~(int64_t)(kEPT - 1); t0 < pe; t0 += kTile) {
-            if (t0 + 2 * kTile < pe) prefetch_tile(a, t0 + 2 * kTile, pe);
-            part_tile(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
+            if (t0 + 2 * kTile < pe) prefetch_tile(a, t0 + 2 * kTile, pe, kPts3);
+            part_tile<kPts3>(a, g, bk, pp, t0, p, pe, &a.sel[g.j].curL, wtot, wbase, fuse ? fh : nullptr, bkc, dn);
         }
         __syncthreads();
         if (fuse) {
@@ -875,7 +878,8 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         }
         {
             ProfScope ps(stream, "part", alg);
-            level_part_kernel<<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
+            if (a.pts3 != nullptr) level_part_kernel<true><<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
+            else level_part_kernel<false><<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         {
