@@ -283,8 +283,8 @@ __device__ __forceinline__ void sf_block_minmax(uint32_t &mn, uint32_t &mx, uint
 // two.  Returns false (in every thread) if a bucket holds more than
 // kSfMaxBucket points: the tile is then left to the select finisher (or, for
 // a balanced tile, which has none, the coordinate is sorted outright).
-template <int NT>
-__device__ bool sort_coord(const SfSmem &sm, uint32_t *red, int T, int k, int nb, uint32_t n, int c, int nseg,
+template <int NT, int nseg>
+__device__ bool sort_coord(const SfSmem &sm, uint32_t *red, int T, int k, int nb, uint32_t n, int c,
                            const uint8_t *code, const uint32_t *fxp, bool bal) {
     constexpr int NW = NT / 32, E = kSfPPT;
     const uint32_t tid = threadIdx.x;
@@ -377,8 +377,10 @@ __device__ bool sort_coord(const SfSmem &sm, uint32_t *red, int T, int k, int nb
         }
     }
     __syncthreads();
-    // rank inside the bucket under the super key of c; the held points step
-    // through their buckets together, so their loads overlap
+    // rank inside the bucket under the super key of c: compared with the
+    // bucket's other points (every slot but the point's own arrival slot);
+    // the held points step through their buckets together, so their loads
+    // overlap
     uint32_t kq[E], rank[E], smax = 0u;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
@@ -386,19 +388,18 @@ __device__ bool sort_coord(const SfSmem &sm, uint32_t *red, int T, int k, int nb
         const uint32_t sz = st[i] >> 16;
         rank[i] = 0u;
         kq[i] = sz > 1u ? kc[q] : 0u;
-        if (sz > 1u) smax = max(smax, sz);
+        if (sz > 1u) smax = max(smax, sz - 1u);
     }
     for (uint32_t j = 0; j < smax; ++j) {
 #pragma unroll
         for (int i = 0; i < E; ++i) {
             const uint32_t sz = st[i] >> 16;
-            if (j < sz && sz > 1u) {
+            if (j + 1u < sz) {
                 const uint32_t q = tid + (uint32_t)i * NT;
-                const uint32_t o = sm.stage[((st[i] & 0xffffu) + j) & tmask0];
+                const uint32_t jj = j < (pk[i] & 0xffu) ? j : j + 1u;  // skip the own slot
+                const uint32_t o = sm.stage[((st[i] & 0xffffu) + jj) & tmask0];
                 const uint32_t ko = kc[o];
-                rank[i] += (ko < kq[i] || (ko == kq[i] && o != q && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q)))
-                               ? 1u
-                               : 0u;
+                rank[i] += (ko < kq[i] || (ko == kq[i] && sk_less_tail(sm.keys, sm.idx, T, k, c, o, q))) ? 1u : 0u;
             }
         }
     }
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
     bool fail = false;
     for (int c = 0; c < k; ++c) {
         if (segs && c != a.l0 % 3) continue;
-        if (!sort_coord<NT>(sm, red, T, k, nb, n, c, 1, nullptr, nullptr, bal)) {
+        if (!sort_coord<NT, 1>(sm, red, T, k, nb, n, c, nullptr, nullptr, bal)) {
             fail = true;
             break;
         }
@@ -551,7 +552,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
         if (segs) {
             if (tid < 3u)
                 fxp[tid] = tid == 0u ? tile_pos(bal, 0u, 0, h, Mt, n) : (h >= 2 ? tile_pos(bal, tid - 1u, 1, h, Mt, n) : 0u);
-            for (int l = 0; l < last && l < 2; ++l) {
+#pragma unroll
+            for (int l = 0; l < 2; ++l) {
+                if (l >= last) break;
                 const int dl = (a.l0 + l) % 3, c = (a.l0 + l + 1) % 3;  // d_l, d_{l+1}
                 // A': segment codes from d_l -- level 0: 0 left, 1 right, 4
                 //     the root; level 1: 2 * (level-0 side) + side, 5 / 6 the
@@ -571,7 +574,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __
                     }
                 }
                 __syncthreads();
-                if (!sort_coord<NT>(sm, red, T, k, nb, n, c, 2 << l, sm.segtab, fxp, bal)) {
+                const bool ok = l == 0 ? sort_coord<NT, 2>(sm, red, T, k, nb, n, c, sm.segtab, fxp, bal)
+                                       : sort_coord<NT, 4>(sm, red, T, k, nb, n, c, sm.segtab, fxp, bal);
+                if (!ok) {
                     if (tid == 0) a.fallback[tile] = 1;  // crowded: the select finisher takes the tile
                     return;
                 }
