@@ -288,7 +288,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kEPT; ++i) r[i] = any ? __ldg(a.src + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < kEPT; ++i) r[i] = any ? __ldcs(a.src + q0 + i) : make_uint4(0u, 0u, 0u, 0u);
     }
     uint32_t kx[kEPT];
 #pragma unroll
@@ -379,7 +379,7 @@ __device__ void part_tile(const LevelArgs &a, const SegInfo &g, const Bucketer &
 #pragma unroll
     for (int i = 0; i < kEPT; ++i) {
         if (side[i] == 0 || side[i] == 2) {
-            a.dst[pos[i]] = r[i];
+            __stcs(a.dst + pos[i], r[i]);  // not read again before the next level's pass: evict first
             if (fh != nullptr && dn < 4) atomicAdd(&fh[(side[i] == 0 ? 0 : kBuckets) + bkc(u4_word(r[i], dn))], 1u);
         } else if (side[i] == 1) {
             a.cand[pos[i]] = r[i];
