@@ -14,13 +14,14 @@ namespace kdt {
 __device__ int g_device_status;
 
 __global__ void status_fold_kernel(const int *s) {
+    pdl_enter();
     const int v = *s;
     if (v != 0) atomicCAS(&g_device_status, 0, v);
 }
 
 void enqueue_status_fold(int *status, cudaStream_t stream) {
     ProfScope ps(stream, "status_fold", 0.0);
-    status_fold_kernel<<<1, 1, 0, stream>>>(status);
+    launch_pdl(status_fold_kernel, 1, 1, 0, stream, status);
 }
 
 int *device_status_address() {

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
                                                             int k, int64_t ld, uint4 *__restrict__ rec,
                                                             uint32_t *__restrict__ bbox,
                                                             int *__restrict__ status) {
+    pdl_enter();
     uint32_t mn[KM], mx[KM];
 #pragma unroll
     for (int c = 0; c < KM; ++c) {
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__
                                                                  uint4 *__restrict__ rec, uint32_t *__restrict__ col0,
                                                                  uint32_t *__restrict__ bbox,
                                                                  int *__restrict__ status) {
+    pdl_enter();
     uint32_t mn[3] = {0xffffffffu, 0xffffffffu, 0xffffffffu}, mx[3] = {0u, 0u, 0u};
     int bad = 0;
     const int64_t groups = N >> 2;  // groups of four points
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__
 
 // Root node table entry: domain = bounding box of all points, dim = widest.
 __global__ void root_table_kernel(const uint32_t *bbox, int k, float *dom, int *dim) {
+    pdl_enter();
     float lo[kMaxK], hi[kMaxK];
     for (int c = 0; c < k; ++c) {
         lo[c] = key2f(bbox[c]);
@@ -341,25 +344,25 @@ int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t 
             const int64_t cap3 = (int64_t)(sms > 0 ? sms : 152) * 16;
             if (g3 > cap3) g3 = cap3;
             if (g3 < 1) g3 = 1;
-            init3_kernel<<<(unsigned)g3, kInit3Threads, 0, stream>>>(pts, S.N, b.pts3 ? nullptr : b.rec[0], col0,
+            launch_pdl(init3_kernel, (unsigned)g3, kInit3Threads, 0, stream, pts, S.N, b.pts3 ? nullptr : b.rec[0], col0,
                                                                     b.bbox, b.status);
         } else if (k <= 3)
-            init_kernel<4><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+            launch_pdl(init_kernel<4>, (unsigned)blocks, kInitThreads, 0, stream, pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);
         else if (k <= 8)
-            init_kernel<8><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+            launch_pdl(init_kernel<8>, (unsigned)blocks, kInitThreads, 0, stream, pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                           b.status);
         else if (k <= 16)
-            init_kernel<16><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+            launch_pdl(init_kernel<16>, (unsigned)blocks, kInitThreads, 0, stream, pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                            b.status);
         else
-            init_kernel<32><<<(unsigned)blocks, kInitThreads, 0, stream>>>(pts, S.N, k, p.ld, b.rec[0], b.bbox,
+            launch_pdl(init_kernel<32>, (unsigned)blocks, kInitThreads, 0, stream, pts, S.N, k, p.ld, b.rec[0], b.bbox,
                                                                            b.status);
         KDT_LAUNCH_CHECK();
     }
     {
         ProfScope ps(stream, "root_table", 0.0);
-        root_table_kernel<<<1, 1, 0, stream>>>(b.bbox, k, b.dom[0], b.dim[0]);
+        launch_pdl(root_table_kernel, 1, 1, 0, stream, b.bbox, k, b.dom[0], b.dim[0]);
         KDT_LAUNCH_CHECK();
     }
     int src = 0;

@@ -473,6 +473,7 @@ __device__ void lane_finish(const FinArgs &a, const FinSmem &sm, int64_t s0, int
 }
 
 __global__ void __launch_bounds__(kFinThreads, 2) finisher_kernel(FinArgs a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char fin_smem[];
     __shared__ SelState st[kFinWarps];
     __shared__ uint32_t red[kFinWarps][64];
@@ -612,7 +613,7 @@ int launch_select_finisher(const Plan &p, const Buffers &b, int src, int32_t *pe
                              (int)p.tp.smem_select) != cudaSuccess)
         return KDT_ECUDA;
     const int64_t ntiles = nodes_on_level(S, p.finish_level);
-    finisher_kernel<<<(unsigned)ntiles, kFinThreads, p.tp.smem_select, stream>>>(a);
+    launch_pdl(finisher_kernel, (unsigned)ntiles, kFinThreads, p.tp.smem_select, stream, a);
     if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
     return KDT_OK;
 }

@@ -55,6 +55,7 @@ constexpr int kSfMaxBucket = 16;   // larger buckets leave the tile to the selec
 constexpr size_t kSfSmemBudget = 110 * 1024;   // two CTAs of up to 512 threads per SM
 constexpr size_t kSfSmemBudget1 = 224 * 1024;  // one 1024-thread CTA per SM (T = 8192)
 constexpr int kMaxLevels = 32;
+constexpr int kSelectOnlyMinK = 5;  // split-widest tiles with this many dimensions go to the select finisher
 constexpr uint32_t kSegHead = 0x80000000u;  // scan word: a node range starts inside the scanned span
 
 struct SfArgs {
@@ -430,6 +431,7 @@ __device__ __forceinline__ uint32_t ids_at(const uint4 &v, int e) {
 // each coordinate array once every three levels).
 template <int NT, bool RR, bool K3>
 __global__ void __launch_bounds__(NT, 1024 / NT) sorted_finisher_kernel(const __grid_constant__ SfArgs a) {
+    pdl_enter();
     constexpr int NW = NT / 32, E = kSfPPT;
     static_assert(!K3 || RR, "the k = 3 schedule is a round-robin one");
     extern __shared__ __align__(16) unsigned char sf_smem[];
@@ -892,7 +894,7 @@ static int launch_sorted_mode(const SfArgs &a, int64_t ntiles, size_t smem, cuda
     if (cudaFuncSetAttribute(sorted_finisher_kernel<NT, RR, K3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return KDT_ECUDA;
-    sorted_finisher_kernel<NT, RR, K3><<<(unsigned)ntiles, NT, smem, stream>>>(a);
+    launch_pdl(sorted_finisher_kernel<NT, RR, K3>, (unsigned)ntiles, NT, smem, stream, a);
     return cudaGetLastError() == cudaSuccess ? KDT_OK : KDT_ECUDA;
 }
 
@@ -906,6 +908,14 @@ static int launch_sorted(const SfArgs &a, int64_t ntiles, size_t smem, cudaStrea
 int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cudaStream_t stream) {
     const Shape &S = p.S;
     if (S.L > kMaxLevels) return KDT_EINVAL;
+    // Split-widest with k >= 5: a presorted tile would move its k - 1 other
+    // arrays on every level; one rank select per node is cheaper there
+    // (measured, 4M uniform points: k = 5 1.02 vs 1.14 ms, k = 8 1.52 vs
+    // 1.85 ms; k = 3: 0.94 vs 0.61 ms the other way).
+    if (p.mode == KDT_SPLIT_WIDEST && p.k >= kSelectOnlyMinK && S.kind == kShapeLeftBalanced) {
+        ProfScope ps(stream, "finisher_select", 0.0);
+        return launch_select_finisher(p, b, src, perm, nullptr, stream);
+    }
     SfArgs a;
     a.S = S;
     a.k = p.k;

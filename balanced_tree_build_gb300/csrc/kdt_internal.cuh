@@ -17,6 +17,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "kdtree_build.h"
@@ -159,6 +160,34 @@ __host__ __device__ __forceinline__ int64_t nodes_on_level(const Shape &S, int l
     return left < w ? left : w;
 }
 
+// ---- programmatic dependent launch ----------------------------------------------
+// The build's kernels are launched so that each may be scheduled while the
+// one before it drains (its launch and setup overlap that tail).  Every such
+// kernel calls pdl_enter() first: it waits until the kernel before it has
+// completed and its writes are visible (so, transitively, everything before
+// that), then lets the kernel after it be scheduled.
+
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---- order-preserving float keys -------------------------------------------
 // Unsigned comparison of the keys equals IEEE '<' on finite floats, with -0
 // folded onto +0 so that the two zeros compare equal (as '<' does).
@@ -241,6 +270,7 @@ struct SegSel {
 
 constexpr int kBuckets = 2048;         // value buckets per subtree on global levels
 constexpr int kBuckets0 = 16384;       // value buckets of level 0 (one subtree, its own histogram pass)
+constexpr int64_t kBuckets0Min = 1 << 24;  // ... from this many points on (below, kBuckets: the pass is latency-bound)
 constexpr int kMultiMaxSegs = 1024;    // multi-CTA levels: at most this many subtrees
 
 struct Plan {

@@ -131,7 +131,7 @@ struct LevelArgs {
     float *dom_nxt;
     int *dim_nxt;
     uint32_t *hist_cur;  // [subtrees][nbk] (multi-CTA levels)
-    int nbk;             // buckets of this level's histogram (kBuckets0 on level 0, else kBuckets)
+    int nbk;             // buckets of this level's histogram (kBuckets0 on level 0 of a large build, else kBuckets)
     uint32_t *hist_nxt;  // children's histograms (fused next level) or null
     SegSel *sel;
     int hist_in;         // per-subtree levels: this level's histograms were built by the level above
@@ -575,6 +575,7 @@ __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64
 // ---- multi-CTA pipeline kernels ----------------------------------------------
 
 __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
+    pdl_enter();
     extern __shared__ uint32_t hist[];  // [a.nbk]
     __shared__ int stop;
     if (stop_requested(a.status, &stop)) return;
@@ -633,6 +634,7 @@ __device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32
 }
 
 __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
+    pdl_enter();
     __shared__ uint32_t red[64];
     __shared__ PartPlan pp;
     __shared__ int stop;
@@ -656,6 +658,7 @@ __device__ __forceinline__ PartPlan part_plan(const SegInfo &g, uint32_t bstar, 
 // kPts3: level 0 reads the k = 3 input points in place of records (a.pts3).
 template <bool kPts3>
 __global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(LevelArgs a) {
+    pdl_enter();
     __shared__ uint32_t wtot[2 * 32], wbase[2 * 32];
     __shared__ uint32_t fh[2 * kBuckets];
     __shared__ int stop;
@@ -695,6 +698,7 @@ __global__ void __launch_bounds__(kPartThreads, kPartCtas) level_part_kernel(Lev
 }
 
 __global__ void __launch_bounds__(kResThreadsMax) level_resolve_kernel(LevelArgs a) {
+    pdl_enter();
     __shared__ SelState st;
     __shared__ uint32_t hist[kCtaRadixBins];
     __shared__ uint32_t qbuf[kSelList];
@@ -739,6 +743,7 @@ __global__ void __launch_bounds__(kResThreadsMax) level_resolve_kernel(LevelArgs
 // the partition and written out whole (this CTA owns both rows); the
 // resolve then adds the candidates' contributions.
 __global__ void __launch_bounds__(kPartThreads, 8) level_seg_kernel(LevelArgs a) {
+    pdl_enter();
     __shared__ SelState st;
     __shared__ uint32_t hist[kBuckets];
     __shared__ uint32_t fh[2 * kBuckets];
@@ -854,14 +859,14 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         if (!fused_here) {
             // level 0 (one subtree) takes a finer histogram: fewer candidates
             // for the one CTA that resolves its split
-            a.nbk = l == 0 ? kBuckets0 : kBuckets;
+            a.nbk = l == 0 && live >= kBuckets0Min ? kBuckets0 : kBuckets;
             if (cudaMemsetAsync(a.hist_cur, 0, (size_t)nseg * a.nbk * 4, stream) != cudaSuccess) return KDT_ECUDA;
             const size_t hsm = (size_t)a.nbk * 4;
             if (cudaFuncSetAttribute(level_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm) !=
                 cudaSuccess)
                 return KDT_ECUDA;
             ProfScope ps(stream, "hist", 0.0);
-            level_hist_kernel<<<(unsigned)nblk, kLvlThreads, hsm, stream>>>(a);
+            launch_pdl(level_hist_kernel, (unsigned)nblk, kLvlThreads, hsm, stream, a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         // picks: by the level above's resolve when it could (this level's
@@ -869,7 +874,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         // this level's resolve picks for the next level
         if (!fused_here) {
             ProfScope ps(stream, "pick", 0.0);
-            level_pick_kernel<<<(unsigned)nseg, kPickThreads, 0, stream>>>(a);
+            launch_pdl(level_pick_kernel, (unsigned)nseg, kPickThreads, 0, stream, a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         if (a.hist_nxt != nullptr && l + 1 < p.multi_levels) {
@@ -878,16 +883,16 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         }
         {
             ProfScope ps(stream, "part", alg);
-            if (a.pts3 != nullptr) level_part_kernel<true><<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
-            else level_part_kernel<false><<<(unsigned)nblk, kPartThreads, 0, stream>>>(a);
+            if (a.pts3 != nullptr) launch_pdl(level_part_kernel<true>, (unsigned)nblk, kPartThreads, 0, stream, a);
+            else launch_pdl(level_part_kernel<false>, (unsigned)nblk, kPartThreads, 0, stream, a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         {
             ProfScope ps(stream, "resolve", 0.0);
             // many candidates per subtree (the top levels): a wider CTA
-            const double cand = (double)live / (double)nseg / (double)(l == 0 ? kBuckets0 : kBuckets);
+            const double cand = (double)live / (double)nseg / (double)a.nbk;
             const int rt = cand > 4096.0 ? kResThreadsMax : kLvlThreads;
-            level_resolve_kernel<<<(unsigned)nseg, rt, 0, stream>>>(a);
+            launch_pdl(level_resolve_kernel, (unsigned)nseg, rt, 0, stream, a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
     } else {
@@ -896,7 +901,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         a.warp_res = 1;  // cursors in shared memory
         if (l + 1 < p.finish_level && fusable) a.hist_nxt = b.hist[(l + 1) & 1];
         ProfScope ps(stream, "seg", alg);
-        level_seg_kernel<<<(unsigned)nseg, kPartThreads, 0, stream>>>(a);
+        launch_pdl(level_seg_kernel, (unsigned)nseg, kPartThreads, 0, stream, a);
         if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
     }
     return KDT_OK;
