@@ -33,6 +33,37 @@ constexpr int kInitThreads = 256;
 
 constexpr int kInitPPT = 4;  // points per thread per iteration
 
+// Folds every thread's per-coordinate key minima and maxima (k <= KM) into
+// the CTA's, then into bbox: one global atomic per coordinate and CTA (the
+// bounding box's 2k words would otherwise take one per warp each).
+template <int KM>
+__device__ __forceinline__ void bbox_fold(const uint32_t (&mn)[KM], const uint32_t (&mx)[KM], int k,
+                                          uint32_t *bbox) {
+    __shared__ uint32_t smn[KM], smx[KM];
+    const uint32_t t = threadIdx.x;
+    if (t < (uint32_t)KM) {
+        smn[t] = 0xffffffffu;
+        smx[t] = 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < KM; ++c) {
+        if (c < k) {
+            const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
+            const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
+            if ((t & 31u) == 0u) {
+                atomicMin(&smn[c], a);
+                atomicMax(&smx[c], b);
+            }
+        }
+    }
+    __syncthreads();
+    if (t < (uint32_t)k) {
+        atomicMin(&bbox[t], smn[t]);
+        atomicMax(&bbox[k + t], smx[t]);
+    }
+}
+
 // KM: compile-time bound on k (4, 8, 16 or 32), so that the per-dimension
 // minima and maxima stay in registers without reserving 2 * KDT_MAX_K of them
 // for small k.  Each point's record (keys, then its input index) is written
@@ -87,6 +118,40 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
                     rec[i] = r[u];
                 }
             }
+        } else if ((k & 3) == 0 && (reinterpret_cast<uintptr_t>(pts) & 15u) == 0) {
+            // k a multiple of 4, points 16-byte aligned: each group of four
+            // keys is one 128-bit load, all of them issued before the stores
+            constexpr int GM = KM / 4;
+            const int gk = k >> 2;
+            const uint4 *p4 = reinterpret_cast<const uint4 *>(pts);
+            uint4 v[kInitPPT][GM];
+#pragma unroll
+            for (int u = 0; u < kInitPPT; ++u) {
+                const int64_t i = i0 + u * nt;
+#pragma unroll
+                for (int g = 0; g < GM; ++g) v[u][g] = g < gk && i < N ? __ldg(p4 + i * gk + g) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kInitPPT; ++u) {
+                const int64_t i = i0 + u * nt;
+                if (i >= N) continue;
+#pragma unroll
+                for (int g = 0; g < GM; ++g) {
+                    if (g >= gk) break;
+                    uint4 r;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float f = __uint_as_float(u4_word(v[u][g], j));
+                        bad |= !isfinite(f);
+                        const uint32_t key = f2key(f);
+                        mn[4 * g + j] = min(mn[4 * g + j], key);
+                        mx[4 * g + j] = max(mx[4 * g + j], key);
+                        u4_set(r, j, key);
+                    }
+                    rec[(int64_t)g * ld + i] = r;
+                }
+                rec[(int64_t)gk * ld + i] = make_uint4((uint32_t)i, 0u, 0u, 0u);  // word k: the index
+            }
         } else {
             // words 0..k of each record: keys, then the index; a group is
             // stored once its four words (or the last, word k) are set
@@ -119,17 +184,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(const float *__restr
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
-#pragma unroll
-    for (int c = 0; c < KM; ++c) {
-        if (c < k) {
-            const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
-            const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
-            if ((threadIdx.x & 31) == 0) {
-                atomicMin(&bbox[c], a);
-                atomicMax(&bbox[k + c], b);
-            }
-        }
-    }
+    bbox_fold<KM>(mn, mx, k, bbox);
 }
 
 // k = 3, points 16-byte aligned: four points are three 128-bit loads, and two
@@ -203,15 +258,7 @@ __global__ void __launch_bounds__(kInit3Threads, 4) init3_kernel(const float *__
         if (col0) col0[tail] = r.x;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(status, KDT_ENONFINITE);
-#pragma unroll
-    for (int c = 0; c < 3; ++c) {
-        const uint32_t a = __reduce_min_sync(0xffffffffu, mn[c]);
-        const uint32_t b = __reduce_max_sync(0xffffffffu, mx[c]);
-        if ((threadIdx.x & 31) == 0) {
-            atomicMin(&bbox[c], a);
-            atomicMax(&bbox[3 + c], b);
-        }
-    }
+    bbox_fold<3>(mn, mx, 3, bbox);
 }
 
 // Root node table entry: domain = bounding box of all points, dim = widest.
