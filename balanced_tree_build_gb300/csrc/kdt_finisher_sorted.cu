@@ -937,7 +937,12 @@ int enqueue_finisher(const Plan &p, const Buffers &b, int src, int32_t *perm, cu
     // subtrees of 2B-1 points, one of B-1+rem, the rest B-1.
     const int Ts = a.T / 2;
     int64_t nbig = ntiles;
-    if (Ts >= 512 && S.kind != kShapeBalanced) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 152;
+    // (with no more tiles than SMs, one launch runs them all side by side)
+    if (Ts >= 512 && S.kind != kShapeBalanced && ntiles > sms) {
         const int lgB = S.L - 1 - p.finish_level;
         const int64_t B = (int64_t)1 << lgB, q = S.M >> lgB, rem = S.M - (q << lgB);
         if (B - 1 <= Ts) {
