@@ -34,6 +34,7 @@ namespace kdt {
 constexpr int kLvlThreads = 512;
 constexpr int kResThreadsMax = 1024;  // resolve CTAs of subtrees with many candidates
 constexpr uint32_t kSelList = 2048;   // listed candidates of a resolve CTA's select
+constexpr int64_t kHistPoints = 16384;  // histogram pass: points per CTA at least
 constexpr int kPickThreads = 256;
 constexpr int kEPT = 4;                          // consecutive points per thread per tile (divides 8: rows up to
                                                  // the next multiple of 8 exist in every record buffer)
@@ -866,7 +867,16 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
                 cudaSuccess)
                 return KDT_ECUDA;
             ProfScope ps(stream, "hist", 0.0);
-            launch_pdl(level_hist_kernel, (unsigned)nblk, kLvlThreads, hsm, stream, a);
+            // every CTA flushes its whole histogram row with global atomics:
+            // at least kHistPoints points per CTA, and no more CTAs than fit
+            // the SMs at once
+            LevelArgs ah = a;
+            const int64_t per_sm = std::min<int64_t>(2048 / kLvlThreads, (int64_t)(227 * 1024) / ((int64_t)hsm + 1024));
+            int64_t gh = (live + kHistPoints - 1) / kHistPoints;
+            gh = std::max<int64_t>(1, std::min<int64_t>(gh, (int64_t)sms * std::max<int64_t>(1, per_sm)));
+            ah.per_cta = (live + gh - 1) / gh;
+            gh = (live + ah.per_cta - 1) / ah.per_cta;
+            launch_pdl(level_hist_kernel, (unsigned)gh, kLvlThreads, hsm, stream, ah);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
         }
         // picks: by the level above's resolve when it could (this level's
