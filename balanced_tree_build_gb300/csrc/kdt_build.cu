@@ -362,7 +362,7 @@ int enqueue_build(const Plan &p, const Buffers &b_in, const float *pts, int32_t 
     const Shape &S = p.S;
     const int k = p.k;
     const double Nd = (double)S.N;
-    if (cudaMemsetAsync(b.status, 0, sizeof(int), stream) != cudaSuccess) return KDT_ECUDA;
+    if (cudaMemsetAsync(b.status, 0, 2 * sizeof(int), stream) != cudaSuccess) return KDT_ECUDA;  // status, level-0 done count
     if (S.kind == kShapeBalanced) {  // heap slots of empty subtrees read -1
         const size_t slots = (((size_t)1) << S.L) - 1;
         if (cudaMemsetAsync(perm, 0xff, slots * sizeof(int32_t), stream) != cudaSuccess) return KDT_ECUDA;

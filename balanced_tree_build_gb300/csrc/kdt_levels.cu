@@ -148,6 +148,7 @@ struct LevelArgs {
     SegSel *sel_next;      // the next level's selections
     uint32_t *hist_nn;     // histograms of the level after next (cleared for the grandchildren), or null
     int *status;
+    int *done;           // histogram pass of a one-subtree level: CTAs finished (the last one picks), or null
     int64_t per_cta;     // positions per CTA (persistent multi-CTA kernels)
     int64_t ld;          // records per group column
 };
@@ -575,6 +576,11 @@ __device__ __forceinline__ void hist_range(const uint32_t *col, int64_t b, int64
 
 // ---- multi-CTA pipeline kernels ----------------------------------------------
 
+__device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32_t *red);
+
+// Histogram of each subtree's split coordinate over its value buckets.  With
+// a.done set (a level of one subtree) the CTA that finishes last also picks
+// the split bucket: the others' counts are in the histogram by then.
 __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
     pdl_enter();
     extern __shared__ uint32_t hist[];  // [a.nbk]
@@ -602,6 +608,19 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
             if (hist[b]) atomicAdd(&H[b], hist[b]);
         __syncthreads();
         p = pe;
+    }
+    if (a.done != nullptr) {
+        __shared__ int last;
+        __shared__ uint32_t red[64];
+        __shared__ PartPlan pp;
+        __threadfence();  // this CTA's counts are in the histogram before it counts itself done
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            pick_subtree(a, full_nodes(a.l), pp, red);
+        }
     }
 }
 
@@ -841,6 +860,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
     a.hist_nn = nullptr;
     a.sel = b.sel[l & 1];
     a.status = b.status;
+    a.done = nullptr;
     a.per_cta = 0;
     a.ld = p.ld;
     const int64_t nseg = nodes_on_level(S, l);
@@ -871,6 +891,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
             // at least kHistPoints points per CTA, and no more CTAs than fit
             // the SMs at once
             LevelArgs ah = a;
+            if (nseg == 1) ah.done = b.status + 1;  // zeroed with the status word at the start of the build
             const int64_t per_sm = std::min<int64_t>(2048 / kLvlThreads, (int64_t)(227 * 1024) / ((int64_t)hsm + 1024));
             int64_t gh = (live + kHistPoints - 1) / kHistPoints;
             gh = std::max<int64_t>(1, std::min<int64_t>(gh, (int64_t)sms * std::max<int64_t>(1, per_sm)));
@@ -882,7 +903,7 @@ int enqueue_level(const Plan &p, const Buffers &b, int l, int src, int32_t *perm
         // picks: by the level above's resolve when it could (this level's
         // histograms were fused there), else by their own kernel; likewise
         // this level's resolve picks for the next level
-        if (!fused_here) {
+        if (!fused_here && nseg > 1) {  // one subtree: picked by the histogram pass
             ProfScope ps(stream, "pick", 0.0);
             launch_pdl(level_pick_kernel, (unsigned)nseg, kPickThreads, 0, stream, a);
             if (cudaGetLastError() != cudaSuccess) return KDT_ECUDA;
