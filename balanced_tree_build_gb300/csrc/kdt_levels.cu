@@ -528,14 +528,15 @@ __device__ void resolve_segment(const LevelArgs &a, const SegInfo &g, const Part
 // Picks the bucket holding rank m from a histogram of nb counts (CTA-wide;
 // nb a multiple of the CTA size).  Returns false if the counts do not add up
 // to n.
-__device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out,
-                            int nb = kBuckets) {
-    const uint32_t tid = threadIdx.x, nt = blockDim.x;
+template <class G>
+__device__ bool pick_bucket_g(const G &grp, const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out,
+                              int nb) {
+    const uint32_t tid = grp.tid(), nt = grp.size();
     const uint32_t per = (uint32_t)nb / nt;
     uint32_t sum = 0;
     for (uint32_t i = 0; i < per; ++i) sum += H[tid * per + i];
     uint32_t total;
-    const uint32_t excl = group_exclusive_scan(CtaGroup{}, sum, red, total);
+    const uint32_t excl = group_exclusive_scan(grp, sum, red, total);
     if (m >= excl && m < excl + sum) {
         uint32_t c = excl;
         for (uint32_t i = 0; i < per; ++i) {
@@ -550,8 +551,13 @@ __device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t 
             c += h;
         }
     }
-    __syncthreads();
+    grp.sync();
     return total == n;
+}
+
+__device__ bool pick_bucket(const uint32_t *H, uint32_t n, uint32_t m, uint32_t *red, PartPlan *out,
+                            int nb = kBuckets) {
+    return pick_bucket_g(CtaGroup{}, H, n, m, red, out, nb);
 }
 
 // Histogram of the bucket function over word d of records [b, e) into shared
@@ -628,14 +634,16 @@ __global__ void __launch_bounds__(kLvlThreads) level_hist_kernel(LevelArgs a) {
 // (a.nbk buckets), written to a.sel[j] with cleared cursors; with a.hist_nxt
 // set, the children's histogram rows of the next level are cleared too.
 // `pp` and `red` are shared scratch.
-__device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32_t *red) {
+template <class G>
+__device__ void pick_subtree_g(const G &grp, const LevelArgs &a, int64_t s, PartPlan &pp, uint32_t *red) {
+    const uint32_t tid = grp.tid();
     const SegInfo g = seg_info(a, s);
-    const bool ok = pick_bucket(a.hist_cur + g.j * a.nbk, g.n, g.m, red, &pp, a.nbk);
+    const bool ok = pick_bucket_g(grp, a.hist_cur + g.j * a.nbk, g.n, g.m, red, &pp, a.nbk);
     // key bounds of the split bucket: two binary searches in two warps
-    if (threadIdx.x == 32) pp.khi = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar + 1u);
-    if (threadIdx.x == 0) pp.klo = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar);
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 32) pp.khi = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar + 1u);
+    if (tid == 0) pp.klo = first_key_at_least(seg_bucketer(a, g.j, g.d, a.nbk), pp.bstar);
+    grp.sync();
+    if (tid == 0) {
         if (!ok) set_status(a.status, KDT_EINTERNAL);
         SegSel sl;
         sl.bstar = pp.bstar;
@@ -648,9 +656,13 @@ __device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32
     }
     if (a.hist_nxt) {
         uint32_t *H = a.hist_nxt + 2 * g.j * kBuckets;
-        for (uint32_t t = threadIdx.x; t < 2u * kBuckets; t += blockDim.x) H[t] = 0u;
+        for (uint32_t t = tid; t < 2u * kBuckets; t += grp.size()) H[t] = 0u;
     }
-    __syncthreads();
+    grp.sync();
+}
+
+__device__ void pick_subtree(const LevelArgs &a, int64_t s, PartPlan &pp, uint32_t *red) {
+    pick_subtree_g(CtaGroup{}, a, s, pp, red);
 }
 
 __global__ void __launch_bounds__(kPickThreads) level_pick_kernel(LevelArgs a) {
@@ -740,7 +752,8 @@ __global__ void __launch_bounds__(kResThreadsMax) level_resolve_kernel(LevelArgs
         // the children's histograms are final now (the part pass flushed its
         // counts before this kernel; this CTA added the candidates'), and so
         // are their domains: pick the next level's split buckets here
-        __shared__ PartPlan ppn;
+        __shared__ PartPlan ppn[2];
+        __shared__ uint32_t redn[2][64];
         __syncthreads();
         LevelArgs an = a;
         an.l = a.l + 1;
@@ -750,8 +763,10 @@ __global__ void __launch_bounds__(kResThreadsMax) level_resolve_kernel(LevelArgs
         an.hist_nxt = a.hist_nn;
         an.sel = a.sel_next;
         an.nbk = kBuckets;
-        pick_subtree(an, 2 * s + 1, ppn, red);
-        pick_subtree(an, 2 * s + 2, ppn, red);
+        // the two children at once, one half of the CTA each (named barriers 1, 2)
+        const uint32_t half = blockDim.x / 2u, hh = threadIdx.x >= half ? 1u : 0u;
+        pick_subtree_g(WarpsGroup{hh * half, half, 1 + (int)hh}, an, 2 * s + 1 + hh, ppn[hh], redn[hh]);
+        __syncthreads();
     }
 }
 
