@@ -876,7 +876,8 @@ int pick_tile(int k, int mode, TilePlan *tp) {
     static const int cands[] = {8192, 4096, 2048, 1024, 512};
     for (int T : cands) {
         const int nb = 2 * T;  // about one point per two buckets
-        const size_t a = sorted_finisher_smem(k, T, mode, nb);
+        // (split-widest with k >= kSelectOnlyMinK never runs the sorted finisher)
+        const size_t a = mode == KDT_SPLIT_WIDEST && k >= kSelectOnlyMinK ? 0 : sorted_finisher_smem(k, T, mode, nb);
         const size_t b = select_finisher_smem(k, T, mode);
         if (a <= (T == 8192 ? kSfSmemBudget1 : kSfSmemBudget) && b <= kSelectSmemMax) {
             tp->tile = T;
