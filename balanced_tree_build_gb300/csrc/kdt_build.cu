@@ -17,8 +17,13 @@
 // 0..F(l+1)-1 (their points go straight to the output), and live subtree s
 // of level l+1 occupies [sb(s, l+1), sb(s, l+1) + ss(s)).
 //
-// Points are carried as records in structure-of-arrays form: k order-
-// preserving coordinate keys plus the input index, double-buffered.
+// Points are carried as 16-byte records: k order-preserving coordinate keys
+// plus the input index, four words per group, G = ceil((k+1)/4) group
+// columns, double-buffered.  With k = 3 points in device memory the first
+// level builds the records itself from the input, so init only reduces the
+// bounding box and writes the first coordinate's keys.  Every build kernel
+// is launched as a programmatic dependent of the one before it
+// (launch_pdl / pdl_enter).
 #include <cstdio>
 
 #include "kdt_internal.cuh"

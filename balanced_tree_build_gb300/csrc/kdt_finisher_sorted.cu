@@ -35,7 +35,9 @@
 //      then each point's rank inside its bucket by comparison under the full
 //      super key.  A bucket of more than kSfMaxBucket points (heavy ties or
 //      clustered values) leaves the whole tile to the select finisher, which
-//      handles any input;
+//      handles any input.  (Round-robin, k = 3, left-balanced tiles: only the
+//      tile root's split coordinate here; the other two are sorted on levels
+//      0 and 1 per subtree, see the k = 3 schedule in step 3);
 //   3. level by level (8 consecutive positions per thread): the side of
 //      every live point (left / split / right, stored as its count
 //      increment) from the array of its node's split coordinate; then each

@@ -20,7 +20,12 @@
 // Step 1 for level l+1 is fused into step 3 of level l when the next split
 // dimension differs from the current one (round-robin rule, k >= 2): the
 // child's domain in that dimension is the parent's, so the child's buckets
-// are known while the parent is partitioned.
+// are known while the parent is partitioned.  Step 2 for level l+1 then runs
+// in the CTA that resolves subtree s on level l (its children's histograms
+// are final once its candidates are added; each half of the CTA picks one
+// child).  Level 0 has a histogram pass of its own, whose last CTA picks.
+// With k = 3 points in device memory, level 0 reads the input points and
+// builds the records in registers.
 //
 // Levels with at most 1024 subtrees are spread over all SMs ("multi-CTA"
 // pipeline: separate histogram / pick / partition / resolve kernels with
