@@ -70,3 +70,21 @@ def test_recorded_traffic_tracks_kernel_source(tmp_path, monkeypatch):
     (src / "kdt_finisher_sorted.cu").write_text("// changed\n")
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.recorded_traffic("finisher") is None
+
+
+def test_reference_arm_json_line(capsys):
+    # the reference arm (the oracle on the host cores) prints the contract's
+    # one JSON line, on the bench workload's config, without a GPU
+    import json
+    rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-sample", "4096"])
+    assert rc == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "uniform_100m" and line["config"]["reference_sample_points"] == 4096
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
