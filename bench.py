@@ -78,19 +78,25 @@ def max_over_ranks(value: float, active: bool, device=None) -> float:
 # clocks during the timed region
 
 class ClockSampler:
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    """nvidia-smi sampling every 20 ms.  It is started before the warm-up
+    (nvidia-smi takes a while to print its first sample) and each sample
+    carries nvidia-smi's own timestamp, so stop() keeps the samples taken
+    inside the timed region (host wall-clock window) and summarises those."""
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_id: str | None):
+    def __init__(self, gpu_id: str | None, interval_ms: int = 20):
         self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines: list[str] = []
         self.thread = None
 
     def start(self):
         cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-               "-lms", "50"]
+               "-lms", str(self.interval_ms)]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -105,7 +111,52 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self) -> dict | None:
+    @staticmethod
+    def _stamp(text: str) -> float | None:
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    @classmethod
+    def summarise(cls, lines: list[str], window: tuple[float, float] | None) -> dict | None:
+        """Median SM clock, max clock and active throttle reasons of the
+        samples inside `window` (host seconds, with one sampling interval of
+        slack); if none falls inside, of the two samples nearest to it."""
+        recs = []
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(cls.FIELDS):
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = {nm for nm, v in zip(cls.REASONS, parts[5:9]) if v.lower() == "active"}
+            recs.append((cls._stamp(parts[0]), sm, smax, reasons))
+        if not recs:
+            return None
+        where = "all samples"
+        sel = recs
+        if window is not None:
+            t0, t1 = window[0] - 0.02, window[1] + 0.02
+            stamped = [r for r in recs if r[0] is not None]
+            inside = [r for r in stamped if t0 <= r[0] <= t1]
+            if inside:
+                sel, where = inside, "timed region"
+            elif stamped:
+                mid = 0.5 * (t0 + t1)
+                sel, where = sorted(stamped, key=lambda r: abs(r[0] - mid))[:2], "nearest to the timed region"
+        reasons = set()
+        for r in sel:
+            reasons |= r[3]
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "samples": len(sel), "window": where, "reasons": sorted(reasons)}
+
+    def stop(self, window: tuple[float, float] | None = None) -> dict | None:
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -115,24 +166,10 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+        try:
+            return self.summarise(list(self.lines), window)
+        except Exception:  # a clock record must never cost the bench line
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
 
 
 def gpu_identifier(dev_index: int) -> str | None:
@@ -438,6 +475,10 @@ def run_ours(args, workload):
     def step():
         kdt.build_tree(pts, workload.mode, out=perm, workspace=ws, stream=stream)
 
+    # clock samples: nvidia-smi starts now, so that it samples by the time
+    # the timed region begins; only samples inside that region are kept
+    sampler = ClockSampler(gpu_identifier(local))
+    sampler.start()
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize(dev)
@@ -447,13 +488,13 @@ def run_ours(args, workload):
 
     # timed region: the library's per-kernel timing is off here
     kdt.profile_enable(False)
-    sampler = ClockSampler(gpu_identifier(local))
     barrier(active)
     torch.cuda.synchronize(dev)
-    sampler.start()
+    t_wall0 = time.time()
     ms = time_steps(step, stream, args.steps)
+    t_wall1 = time.time()
     barrier(active)
-    clocks = sampler.stop()
+    clocks = sampler.stop((t_wall0, t_wall1))
     ms_max = max_over_ranks(ms, active, dev if active else None)
     rc = kdt.status(stream)
     if rc != 0:

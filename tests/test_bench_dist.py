@@ -88,3 +88,25 @@ def test_reference_arm_json_line(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_clock_samples_kept_inside_the_timed_region():
+    # nvidia-smi lines: timestamp, sm, max sm, power, active mask, 4 reasons
+    import datetime
+    base = datetime.datetime(2026, 12, 2, 18, 0, 0)
+
+    def line(ms, sm, reason=("Not Active",) * 4):
+        ts = (base + datetime.timedelta(milliseconds=ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return ", ".join([ts, str(sm), "2070", "900.0", "0x0"] + list(reason))
+
+    t0 = base.timestamp()
+    lines = [line(0, 1200), line(500, 2070), line(520, 2070), line(540, 2070, ("Not Active", "Not Active",
+             "Not Active", "Active")), line(900, 1500)]
+    got = bench.ClockSampler.summarise(lines, (t0 + 0.49, t0 + 0.55))
+    assert got["samples"] == 3 and got["window"] == "timed region"
+    assert got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0 and got["reasons"] == ["sw_power_cap"]
+    # nothing inside: the two samples nearest to the window
+    near = bench.ClockSampler.summarise(lines, (t0 + 0.7, t0 + 0.72))
+    assert near["samples"] == 2 and near["window"] == "nearest to the timed region"
+    # malformed lines are skipped; no usable line gives None
+    assert bench.ClockSampler.summarise(["garbage", ""], None) is None
